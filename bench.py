@@ -1,0 +1,458 @@
+#!/usr/bin/env python3
+"""Benchmark of one continuous-batching attention step over a paged KV cache on GB300.
+
+A step is the whole hot path over one batch: pa_cache_append of the step's new tokens through
+the slot mapping, then pa_attention of every query token over its sequence's paged K/V.  The
+default workload is the 7B-class MHA decode step (32 heads x 128, block 16, 64 sequences with
+contexts uniform in [512, 4096], bf16 K/V); --config picks another of the five named workloads.
+
+Prints one JSON line.  `value` is achieved HBM GB/s of the step (algorithmic bytes: every unique
+K/V block touched once, q read, out written, metadata, plus the append's reads and writes,
+divided by the device time of the step); attended tokens/s is reported beside it.  Inputs are
+resident in HBM and larger than L2.  `e2e` is the same metric through the public API with the
+step's inputs copied from pinned host memory and the output copied back inside the timed
+region.  `roofline` reports the main attention kernel alone, timed with CUDA events recorded
+around it by the library.  `cpu_baseline` times the fp64 oracle on a bounded sample.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference]
+
+With N > 1 (launched by torchrun) every rank runs an independent replica of the workload on
+its own GPU; there is no collective on the data path ("replicas only").
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged-attn step: achieved HBM GB/s (% of peak), attended tokens/s"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="budget of the oracle CPU-baseline sample")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------------------------------------
+# peaks, clocks
+# ---------------------------------------------------------------------------------------------
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured", j
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback", {}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "", 1).isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "", 1).isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------------------------
+# the workload on the device
+# ---------------------------------------------------------------------------------------------
+class DeviceWorkload:
+    """Pools filled with the workload's prior context, plus the step's inputs, on one GPU."""
+
+    def __init__(self, w, device):
+        import torch
+        import paged_kv_cache_286_gb300 as pa
+        self.pa, self.torch, self.w, self.device = pa, torch, w, device
+
+        def dev(bits):
+            bits = np.ascontiguousarray(bits)
+            t = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16) \
+                if bits.dtype == np.uint16 else torch.from_numpy(bits)
+            return t.to(device)
+
+        self.host = {  # the step's inputs in pinned host memory (for the end-to-end leg)
+            "q": torch.from_numpy(w.q_bits.view(np.int16)).view(torch.bfloat16),
+            "k": torch.from_numpy(w.k_new_bits.view(np.int16)).view(torch.bfloat16),
+            "v": torch.from_numpy(w.v_new_bits.view(np.int16)).view(torch.bfloat16),
+            "slots": torch.from_numpy(w.slot_mapping),
+            "tables": torch.from_numpy(w.block_tables),
+            "ctx": torch.from_numpy(w.context_lens),
+            "qsl": torch.from_numpy(w.query_start_loc),
+        }
+        self.host = {k: v.contiguous().pin_memory() for k, v in self.host.items()}
+        self.dev = {k: v.to(device) for k, v in self.host.items()}
+        fp8 = w.cache_dtype == "fp8_e4m3"
+        self.k_cache = torch.zeros(w.pool_shape, dtype=torch.uint8 if fp8 else torch.bfloat16,
+                                   device=device)
+        self.v_cache = torch.zeros_like(self.k_cache)
+        self.out = torch.empty((w.num_tokens, w.num_q_heads, w.head_dim), dtype=torch.float32,
+                               device=device)
+        self.out_host = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
+        nbytes = pa.attention_workspace_size(w.num_seqs, w.num_tokens, w.num_q_heads,
+                                             w.num_kv_heads, w.head_dim, w.max_context_len,
+                                             w.max_query_len)
+        self.ws = pa.new_workspace(nbytes, device)
+        P = w.slot_prior.shape[0]
+        for a in range(0, P, 1 << 16):   # set-up: the context cached before the step
+            b = min(P, a + (1 << 16))
+            pa.cache_append(dev(w.k_prior_bits[a:b]), dev(w.v_prior_bits[a:b]),
+                            torch.from_numpy(w.slot_prior[a:b]).to(device), self.k_cache,
+                            self.v_cache, self.ws, k_scale=w.k_scale, v_scale=w.v_scale)
+        torch.cuda.synchronize(device)
+        self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.host.values())
+        self.d2h_bytes = self.out.numel() * self.out.element_size()
+
+    def step(self, t=None):
+        """pa_cache_append + pa_attention on tensors `t` (device copies by default)."""
+        t = self.dev if t is None else t
+        w, pa = self.w, self.pa
+        pa.cache_append(t["k"], t["v"], t["slots"], self.k_cache, self.v_cache, self.ws,
+                        k_scale=w.k_scale, v_scale=w.v_scale)
+        pa.attention(t["q"], self.k_cache, self.v_cache, t["tables"], t["ctx"], t["qsl"],
+                     self.ws, scale=w.scale, max_context_len=w.max_context_len,
+                     max_query_len=w.max_query_len, out=self.out, k_scale=w.k_scale,
+                     v_scale=w.v_scale)
+
+    def step_from_host(self):
+        for k, v in self.host.items():
+            self.dev[k].copy_(v, non_blocking=True)
+        self.step()
+        self.out_host.copy_(self.out, non_blocking=True)
+
+    def launches_per_step(self) -> int:
+        """Our kernels one step launches: append, plan, attention, and the LSE merge when the
+        workspace carries split partials (it does exactly when a sequence can span more than
+        one KV partition)."""
+        w = self.w
+        size = self.pa.attention_workspace_size(w.num_seqs, w.num_tokens, w.num_q_heads,
+                                                w.num_kv_heads, w.head_dim, w.max_context_len,
+                                                w.max_query_len)
+        no_partials = 256 + ((4 * (w.num_seqs + 1) + 255) // 256) * 256
+        return 3 + (1 if size > no_partials else 0)
+
+
+def decode_src_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_286_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profiles(config_id: int):
+    """DRAM bytes per launch of the attention kernel from a committed ncu summary, if it was
+    taken from the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        e = j.get(f"cfg{config_id}")
+        if e and e.get("src_sha") == decode_src_sha():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline and reference arm)
+# ---------------------------------------------------------------------------------------------
+def _oracle_sample_worker(args):
+    """Runs in a spawned process with one BLAS thread: the oracle's whole step (append of the
+    prior context and the new tokens, then attention) on the first `k` sequences."""
+    config_id, k = args
+    sys.path.insert(0, ROOT)
+    from oracle import run_step
+    from synthetic.workloads import config_lengths, make_workload
+    ctx, ql, kw = config_lengths(config_id)
+    w = make_workload(ctx[:k], ql[:k], seed=1000 + config_id, name=f"cfg{config_id}-sample",
+                      **kw)
+    t0 = time.perf_counter()
+    run_step(w)
+    dt = time.perf_counter() - t0
+    return dt, w.algorithmic_bytes() + w.append_bytes(), w.attended_tokens(), k
+
+
+def oracle_sample(config_id: int, seconds: float):
+    """Time the oracle on growing sub-batches of the workload until one takes >= `seconds`/4,
+    then report the largest; returns dict(value GB/s, tokens/s, seqs, seconds)."""
+    from synthetic.workloads import config_lengths
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    ctx, _, _ = config_lengths(config_id)
+    S = len(ctx)
+    ctxmp = mp.get_context("spawn")
+    k, best = 1, None
+    with ctxmp.Pool(1) as pool:
+        while True:
+            dt, nbytes, toks, k = pool.apply(_oracle_sample_worker, ((config_id, k),))
+            best = (dt, nbytes, toks, k)
+            if dt >= seconds / 4 or k >= S:
+                break
+            k = min(S, max(k + 1, int(k * min(4.0, (seconds / 4) / max(dt, 1e-3)))))
+    dt, nbytes, toks, k = best
+    return {"value": nbytes / dt / 1e9, "tokens_per_s": toks / dt, "seqs": k, "of_seqs": S,
+            "seconds": dt}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from synthetic.workloads import CONFIG_NAMES, config_lengths
+    ctx, _, _ = config_lengths(args.config)
+    budget = 150.0 / max(1, args.steps + args.warmup)   # whole run within a few minutes
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    ctxmp = mp.get_context("spawn")
+    with ctxmp.Pool(1) as pool:
+        # size the per-step sample from a one-sequence calibration
+        dt1, _, _, _ = pool.apply(_oracle_sample_worker, ((args.config, 1),))
+        k = max(1, min(len(ctx), int(budget / max(dt1, 1e-3))))
+        times, nbytes, toks = [], 0, 0
+        for i in range(args.warmup + args.steps):
+            dt, nb, tk, _ = pool.apply(_oracle_sample_worker, ((args.config, k),))
+            if i >= args.warmup:
+                times.append(dt)
+                nbytes, toks = nb, tk
+    total = sum(times)
+    value = nbytes * len(times) / total / 1e9
+    sample = (f"first {k} of {len(ctx)} sequences of the workload per step (same recipe), "
+              "fp64 oracle: set-up append, step append and attention")
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / len(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"cfg{args.config}: {CONFIG_NAMES[args.config]}",
+                       "sample_seqs": k},
+            "attended_tokens_per_s": toks * len(times) / total,
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    if args.gpus != world and world > 1:
+        print(f"--gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist = dist_init(world, "nccl")
+    from paged_kv_cache_286_gb300 import build
+    if rank == 0:
+        build.build()
+    barrier(dist, device)
+    import paged_kv_cache_286_gb300 as pa
+    from synthetic.workloads import CONFIG_NAMES, make_config
+
+    w = make_config(args.config)
+    dw = DeviceWorkload(w, device)
+    algo_attn = w.algorithmic_bytes()
+    algo_step = algo_attn + w.append_bytes()
+    stream = torch.cuda.current_stream(device)
+
+    # warm-up (also checks the device error word once)
+    for _ in range(max(3, args.warmup)):
+        dw.step()
+    assert pa.check_error(dw.ws) == 0
+
+    K = args.steps
+    kb = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ka = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for e in kb + ka:       # create the events before handing their handles to the library
+        e.record(stream)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    torch.cuda.synchronize(device)
+    barrier(dist, device)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize(device)
+    start.record(stream)
+    for i in range(K):
+        pa.set_kernel_timing_events(kb[i], ka[i])
+        dw.step()
+    stop.record(stream)
+    torch.cuda.synchronize(device)
+    pa.set_kernel_timing_events(None, None)
+    barrier(dist, device)
+    clk = clocks.stop()
+    step_ms = start.elapsed_time(stop) / K
+    kern_ms = statistics.mean(kb[i].elapsed_time(ka[i]) for i in range(K))
+    step_ms = max_over_ranks(step_ms, dist, device)
+
+    # end to end: inputs from pinned host memory, output back, every step
+    for _ in range(2):
+        dw.step_from_host()
+    torch.cuda.synchronize(device)
+    barrier(dist, device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        dw.step_from_host()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K, dist, device)
+    assert pa.check_error(dw.ws) == 0
+
+    peak, peak_kind, _ = load_peaks()
+    value = world * algo_step / (step_ms * 1e-3) / 1e9
+    achieved = algo_attn / (kern_ms * 1e-3) / 1e9
+    result = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline:
+            s = oracle_sample(args.config, args.cpu_seconds)
+            cpu = {"value": s["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
+                   "sample": f"first {s['seqs']} of {s['of_seqs']} sequences of the workload "
+                             f"(same recipe), fp64 oracle step (set-up append, step append, "
+                             f"attention), {s['seconds']:.1f} s on one host core",
+                   "tokens_per_s": s["tokens_per_s"]}
+        result = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3" if w.cache_dtype == "fp8_e4m3" else "bf16", "data": "synthetic",
+            "config": {"workload": f"cfg{args.config}: {CONFIG_NAMES[args.config]}",
+                       "l2": f"no flush: each step streams {algo_attn / 1e9:.2f} GB of K/V "
+                             "and q/out, far above the 129 MB L2",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "hbm_frac_of_peak": value / world / peak,
+            "attended_tokens_per_s": world * w.attended_tokens() / (step_ms * 1e-3),
+            "algorithmic_bytes_per_step": algo_step,
+            "e2e": {"value": world * algo_step / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+                    "h2d_bytes_per_step": dw.h2d_bytes, "d2h_bytes_per_step": dw.d2h_bytes,
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": K * dw.launches_per_step(),
+            "roofline": {"bound": "hbm", "kernel": "decode_kernel (split-KV paged attention)",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
+                         "traffic": traffic_from_profiles(args.config),
+                         "algorithmic_bytes_per_launch": algo_attn,
+                         "kernel_ms": kern_ms},
+            "cpu_baseline": cpu,
+            "clocks": clk,
+        }
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,676 @@
+// Split-KV paged attention for decode tokens and short query runs, plus its log-sum-exp merge.
+//
+// What it computes ("Serving LLMs with vLLM: Continuous Batching and PagedAttention Explained",
+// section "Attention Over Scattered Blocks"): for every query token i of sequence s at position
+// p_i and every q head, softmax(scale * q . k_j) over keys j <= p_i, applied to the values, where
+// key/value j live in physical block block_tables[s][j / 16] at offset j % 16.
+//
+// Design (GB300 / sm_103a):
+//  * Work item = (sequence, kv head, tile of 8 rows, KV partition of `pblk` blocks).  A row is a
+//    (query token, q head of the GQA group) pair, so one item loads each K/V block once for the
+//    whole group.  A plan kernel turns context lengths into per-sequence item counts; the
+//    attention kernel is persistent and takes items from an atomic counter.
+//  * Each of the CTA's 4 warps owns every 4th block of the partition and streams it through its
+//    own ring of shared-memory stages: one lane issues 2-D TMA tile copies of the (block, head)
+//    K and V tiles (128-byte swizzle) after reading the block id from the table, completion is
+//    counted on the stage's mbarrier.  The HBM stream is the whole cost of decode.
+//  * Scores and P.V run on warp-level tensor-core MMAs (m16n8k16): S = Q K^T with the 8 rows as
+//    M (padded to 16), and O^T = V^T P^T so that the probabilities feed the second MMA straight
+//    from the first one's accumulators.  bf16 caches: P is split into bf16 hi + lo parts, which
+//    keeps P exact to ~2^-16.  E4M3 caches: K and V are converted to f16 in registers (exact),
+//    q is scaled by a power of two per row into f16 range, P is f16.
+//  * Online softmax in the log2 domain per warp; the 4 warps' (m, l, O) are merged in shared
+//    memory; an item that covers the whole sequence writes `out`, otherwise it writes a
+//    normalised partial and its log-sum-exp, which the merge kernel combines.
+#include <math_constants.h>
+
+#include <algorithm>
+
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+struct DecodeParams {
+  const __nv_bfloat16* q;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const int32_t* qsl;
+  int32_t* item_start;
+  float* part_lse;
+  float* part_o;
+  void* out;
+  WsHeader* hdr;
+  int32_t max_blocks_per_seq;
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t group;           // q heads per kv head
+  int32_t num_blocks;
+  int32_t max_context_len;
+  int32_t max_query_len;
+  int32_t pblk;
+  int32_t pmax;
+  int32_t decode_max_query;
+  int32_t out_bf16;
+  float score_log2;        // scale * log2(e) (* k_scale for E4M3)
+  float v_out_scale;       // v_scale for E4M3, else 1
+};
+
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Items of one sequence on the decode path (0 if it belongs to the prefill path or is invalid).
+__device__ __forceinline__ int decode_items_of(const DecodeParams& p, int n, int L, bool* bad) {
+  *bad = false;
+  if (n <= 0) {
+    *bad = (n < 0);
+    return 0;
+  }
+  if (n > L || L > p.max_context_len || n > p.max_query_len ||
+      L > p.max_blocks_per_seq * kBlockSize) {
+    *bad = true;
+    return 0;
+  }
+  if (n > p.decode_max_query) return 0;
+  const int tpt = kRowsPerTile / p.group;  // query tokens per tile
+  const int qtiles = ceil_div(n, tpt);
+  const int nparts = ceil_div(ceil_div(L, kBlockSize), p.pblk);
+  return p.num_kv_heads * qtiles * nparts;
+}
+
+// One CTA: exclusive prefix sum of decode items over sequences; resets the work counters.
+__global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
+  __shared__ int warp_sums[32];
+  __shared__ int carry_s;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) carry_s = 0;
+  __syncthreads();
+  for (int base = 0; base < p.num_seqs; base += 1024) {
+    const int s = base + tid;
+    int cnt = 0;
+    if (s < p.num_seqs) {
+      const int n = p.qsl[s + 1] - p.qsl[s];
+      const int L = p.context_lens[s];
+      bool bad;
+      cnt = decode_items_of(p, n, L, &bad);
+      if (bad) set_error(&p.hdr->error, PA_DEVERR_LENGTHS);
+    }
+    int x = cnt;  // inclusive warp scan
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int w = warp_sums[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      warp_sums[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    const int carry = carry_s;
+    const int excl = carry + (warp ? warp_sums[warp - 1] : 0) + x - cnt;
+    if (s < p.num_seqs) p.item_start[s] = excl;
+    __syncthreads();
+    if (tid == 1023) carry_s = excl + cnt;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    p.item_start[p.num_seqs] = carry_s;
+    p.hdr->decode_counter = 0;
+  }
+}
+
+template <int D, bool kFp8>
+struct DecodeCfg {
+  static constexpr int kElem = kFp8 ? 1 : 2;
+  static constexpr int kTileBytes = kBlockSize * D * kElem;         // one (block, head) tile
+  static constexpr int kBoxCols = kFp8 ? 128 : 64;                  // elements per 128-B row
+  static constexpr int kBoxes = D / kBoxCols;                       // TMA boxes per tile
+  static constexpr int kBoxBytes = kBlockSize * 128;                // 16 rows x 128 B
+  static constexpr int kStageBytes = 2 * kTileBytes;                // K tile + V tile
+  static constexpr int kKSteps = D / 16;
+};
+
+template <int D, bool kFp8, int NST>
+constexpr int decode_smem_bytes() {
+  using C = DecodeCfg<D, kFp8>;
+  return 1024 /*alignment slack*/ + kDecodeWarps * NST * C::kStageBytes +
+         kDecodeWarps * NST * 8 /*mbarriers*/ + 64 /*item slot*/;
+}
+
+struct ItemInfo {
+  int s, h, qt, part, t0, n, L, nparts, blk_begin, blk_end, pos_base, rows, valid;
+};
+
+template <int D, bool kFp8, int NST>
+__global__ void __launch_bounds__(kDecodeWarps * 32)
+    decode_kernel(const __grid_constant__ CUtensorMap kmap,
+                  const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
+  using C = DecodeCfg<D, kFp8>;
+  static_assert(C::kStageBytes * NST >= kRowsPerTile * D * 4 + 2 * kRowsPerTile * 4,
+                "merge scratch must fit in a warp's stage buffers");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kDecodeWarps * NST * C::kStageBytes);
+  ItemInfo* s_item = reinterpret_cast<ItemInfo*>(bars + kDecodeWarps * NST);
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int quad = lane >> 2;  // fragment row group
+  const int qc = lane & 3;     // position within the quad
+  uint8_t* wbuf = smem + warp * NST * C::kStageBytes;
+  uint64_t* wbars = bars + warp * NST;
+
+  if (lane == 0) {
+    for (int st = 0; st < NST; ++st) mbar_init(&wbars[st], 1);
+    fence_barrier_init();
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&vmap);
+  }
+  __syncthreads();
+
+  const int total_items = p.item_start[p.num_seqs];
+  uint32_t it = 0;          // blocks this warp has consumed so far (stage / phase tracking)
+  bool timed_out = false;
+
+  while (true) {
+    if (threadIdx.x == 0) {
+      ItemInfo info;
+      const int item = static_cast<int>(atomicAdd(&p.hdr->decode_counter, 1u));
+      info.valid = item < total_items;
+      if (info.valid) {
+        int lo = 0, hi = p.num_seqs;  // largest s with item_start[s] <= item
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (p.item_start[mid] <= item) lo = mid; else hi = mid;
+        }
+        const int s = lo;
+        const int t0 = p.qsl[s];
+        const int n = p.qsl[s + 1] - t0;
+        const int L = p.context_lens[s];
+        const int tpt = kRowsPerTile / p.group;
+        const int qtiles = ceil_div(n, tpt);
+        const int nblk = ceil_div(L, kBlockSize);
+        const int nparts = ceil_div(nblk, p.pblk);
+        int local = item - p.item_start[s];
+        const int part = local % nparts;
+        local /= nparts;
+        const int qt = local % qtiles;
+        const int h = local / qtiles;
+        const int tok_begin = qt * tpt;
+        const int tok_end = min(n, tok_begin + tpt);
+        const int pos_max = L - n + tok_end - 1;           // last position in the tile
+        const int blk_tile = pos_max / kBlockSize + 1;     // blocks the tile can see
+        info.s = s; info.h = h; info.qt = qt; info.part = part; info.t0 = t0 + tok_begin;
+        info.n = tok_end - tok_begin; info.L = L; info.nparts = nparts;
+        info.blk_begin = min(part * p.pblk, blk_tile);
+        info.blk_end = min((part + 1) * p.pblk, blk_tile);
+        info.pos_base = L - n + tok_begin;                 // position of the tile's first token
+        info.rows = info.n * p.group;
+      }
+      *s_item = info;
+    }
+    const bool any_timeout = __syncthreads_or(timed_out) != 0;
+    const ItemInfo I = *s_item;
+    if (!I.valid || any_timeout) break;
+    const uint32_t it0 = it;  // blocks consumed before this item
+
+    // ---- rows held by this lane: S row `quad`; O^T columns 2*qc, 2*qc+1 ------------------
+    const int row = quad;
+    const bool row_ok = row < I.rows;
+    const int row_tok = row_ok ? row / p.group : 0;
+    const int row_pos = I.pos_base + row_tok;
+    const int pos_last = I.pos_base + I.n - 1;
+
+    // ---- table entries of this warp's blocks, one per lane -----------------------------
+    const int my_first = I.blk_begin + warp;
+    const int nb_w = my_first < I.blk_end ? ceil_div(I.blk_end - my_first, kDecodeWarps) : 0;
+    int phys_lane = -1;
+    if (lane < nb_w) {
+      const int b = my_first + lane * kDecodeWarps;
+      phys_lane = __ldg(p.block_tables + static_cast<int64_t>(I.s) * p.max_blocks_per_seq + b);
+      if (phys_lane < 0 || phys_lane >= p.num_blocks) {
+        set_error(&p.hdr->error, PA_DEVERR_BLOCK_ID);
+        phys_lane = -1;
+      }
+    }
+
+    auto issue = [&](int k) {  // stage load for the warp's k-th block (all lanes call)
+      const int phys = __shfl_sync(0xffffffffu, phys_lane, k);
+      if (lane == 0) {
+        const uint32_t st = (it0 + k) % NST;
+        uint64_t* bar = &wbars[st];
+        if (phys >= 0) {
+          uint8_t* kt = wbuf + st * C::kStageBytes;
+          uint8_t* vt = kt + C::kTileBytes;
+          const int y = (phys * p.num_kv_heads + I.h) * kBlockSize;
+          mbar_arrive_expect_tx(bar, C::kStageBytes);
+#pragma unroll
+          for (int bx = 0; bx < C::kBoxes; ++bx) {
+            tma_load_2d(kt + bx * C::kBoxBytes, &kmap, bx * C::kBoxCols, y, bar);
+            tma_load_2d(vt + bx * C::kBoxBytes, &vmap, bx * C::kBoxCols, y, bar);
+          }
+        } else {
+          mbar_arrive(bar);
+        }
+      }
+    };
+
+    const int npre = min(NST, nb_w);
+    for (int k = 0; k < npre; ++k) issue(k);
+
+    // ---- q fragments (A operand of S = Q K^T), rows 8..15 are zero -----------------------
+    uint32_t qa[C::kKSteps][2];
+    float row_scale = p.score_log2;
+    {
+      const __nv_bfloat16* qrow =
+          p.q + (static_cast<int64_t>(I.t0 + row_tok) * p.num_q_heads + I.h * p.group +
+                 (row_ok ? row % p.group : 0)) * D;
+      if constexpr (!kFp8) {
+#pragma unroll
+        for (int ks = 0; ks < C::kKSteps; ++ks) {
+          if (row_ok) {
+            qa[ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * qc));
+            qa[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * qc));
+          } else {
+            qa[ks][0] = qa[ks][1] = 0u;
+          }
+        }
+      } else {
+        // k index 2c,2c+1 of a k-step <-> d 4c,4c+1; k index 2c+8,2c+9 <-> d 4c+2,4c+3
+        uint2 raw[C::kKSteps];
+        float amax = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < C::kKSteps; ++ks) {
+          raw[ks] = row_ok ? __ldg(reinterpret_cast<const uint2*>(qrow + 16 * ks + 4 * qc))
+                           : make_uint2(0u, 0u);
+          amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16lo_to_f32(raw[ks].x)),
+                                         fabsf(bf16hi_to_f32(raw[ks].x))),
+                                   fmaxf(fabsf(bf16lo_to_f32(raw[ks].y)),
+                                         fabsf(bf16hi_to_f32(raw[ks].y)))));
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        // power of two e with amax * 2^e < 2^15 (f16 range), exact scaling
+        int ex = 0;
+        if (amax > 0.f) frexpf(amax, &ex);
+        const int e = max(-100, min(100, 15 - ex));
+        const float up = ldexpf(1.f, e);
+        row_scale = p.score_log2 * ldexpf(1.f, -e);
+#pragma unroll
+        for (int ks = 0; ks < C::kKSteps; ++ks) {
+          qa[ks][0] = pack_f16x2(bf16lo_to_f32(raw[ks].x) * up, bf16hi_to_f32(raw[ks].x) * up);
+          qa[ks][1] = pack_f16x2(bf16lo_to_f32(raw[ks].y) * up, bf16hi_to_f32(raw[ks].y) * up);
+        }
+      }
+    }
+
+    float m_run = -CUDART_INF_F;  // running max of row `quad`, log2 domain
+    float l_run = 0.f;            // this lane's share of the running sum
+    float oacc[C::kKSteps][4];
+#pragma unroll
+    for (int j = 0; j < C::kKSteps; ++j) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.f;
+
+    for (int k = 0; k < nb_w; ++k) {
+      const uint32_t st = it % NST;
+      const uint32_t parity = (it / NST) & 1u;
+      // every lane polls; the outcome is made warp-uniform before any lane acts on it
+      if (!__all_sync(0xffffffffu, mbar_wait(&wbars[st], parity))) {
+        if (lane == 0) set_error(&p.hdr->error, PA_DEVERR_TIMEOUT);
+        timed_out = true;
+        // drain the other loads in flight, each with its own bounded wait
+        for (int k2 = k + 1; k2 < min(nb_w, k + NST); ++k2)
+          mbar_wait(&wbars[(it + (k2 - k)) % NST], ((it + (k2 - k)) / NST) & 1u);
+        break;
+      }
+      const int phys = __shfl_sync(0xffffffffu, phys_lane, k);
+      if (phys >= 0) {
+        const int blk = my_first + k * kDecodeWarps;
+        const int key0 = blk * kBlockSize;
+        const uint32_t kbase = smem_u32(wbuf + st * C::kStageBytes);
+        const uint32_t vbase = kbase + C::kTileBytes;
+
+        // ---- S = Q K^T for the block's 16 keys (two n-tiles of 8 keys) -------------------
+        float sacc[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+          const int krow = 8 * nt + (lane & 7);
+          if constexpr (!kFp8) {
+#pragma unroll
+            for (int kk = 0; kk < D / 32; ++kk) {
+              const int chunk = 4 * kk + (lane >> 3);  // 16-byte chunk = 8 d
+              const uint32_t addr = kbase + (chunk >> 3) * C::kBoxBytes + krow * 128 +
+                                    (((chunk & 7) ^ (krow & 7)) << 4);
+              uint32_t b0, b1, b2, b3;
+              ldsm_x4(addr, b0, b1, b2, b3);
+              const uint32_t a0[4] = {qa[2 * kk][0], 0u, qa[2 * kk][1], 0u};
+              const uint32_t a1[4] = {qa[2 * kk + 1][0], 0u, qa[2 * kk + 1][1], 0u};
+              mma_bf16(sacc[nt], a0, b0, b1);
+              mma_bf16(sacc[nt], a1, b2, b3);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < D / 64; ++kk) {
+              const int chunk = 4 * kk + (lane >> 3);  // 16-byte chunk = 16 d = one k-step
+              const uint32_t addr = kbase + krow * 128 + (((chunk & 7) ^ (krow & 7)) << 4);
+              uint32_t r[4];
+              ldsm_x4(addr, r[0], r[1], r[2], r[3]);
+#pragma unroll
+              for (int m = 0; m < 4; ++m) {
+                const int ks = 4 * kk + m;
+                const uint32_t a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
+                mma_f16(sacc[nt], a, e4m3x2_to_f16x2(static_cast<uint16_t>(r[m] & 0xffffu)),
+                        e4m3x2_to_f16x2(static_cast<uint16_t>(r[m] >> 16)));
+              }
+            }
+          }
+        }
+
+        // ---- online softmax for row `quad` over keys 8nt + 2qc + e ----------------------
+        float sv[4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int kidx = key0 + 8 * nt + 2 * qc + e;
+            const bool ok = row_ok && kidx <= row_pos;
+            sv[2 * nt + e] = ok ? sacc[nt][e] * row_scale : -CUDART_INF_F;
+          }
+        float mloc = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
+        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
+        const float m_new = fmaxf(m_run, mloc);
+        const float m_use = (m_new == -CUDART_INF_F) ? 0.f : m_new;
+        const float alpha = fast_exp2(m_run - m_use);
+        float pr[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) pr[i] = fast_exp2(sv[i] - m_use);
+        l_run = l_run * alpha + (pr[0] + pr[1]) + (pr[2] + pr[3]);
+        m_run = m_new;
+        const float alpha_a = __shfl_sync(0xffffffffu, alpha, 8 * qc);
+        const float alpha_b = __shfl_sync(0xffffffffu, alpha, 8 * qc + 4);
+#pragma unroll
+        for (int j = 0; j < C::kKSteps; ++j) {
+          oacc[j][0] *= alpha_a;
+          oacc[j][1] *= alpha_b;
+          oacc[j][2] *= alpha_a;
+          oacc[j][3] *= alpha_b;
+        }
+
+        // keys past the tile's last position hold stale slots: zero their V (may be NaN)
+        const int nvalid = min(kBlockSize, pos_last + 1 - key0);
+        uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;  // keys 2qc.., keys 8+2qc..
+        if (nvalid < kBlockSize) {
+          vm_lo = (2 * qc < nvalid ? 0x0000ffffu : 0u) | (2 * qc + 1 < nvalid ? 0xffff0000u : 0u);
+          vm_hi = (8 + 2 * qc < nvalid ? 0x0000ffffu : 0u) |
+                  (9 + 2 * qc < nvalid ? 0xffff0000u : 0u);
+        }
+
+        // ---- O^T += V^T P^T --------------------------------------------------------------
+        if constexpr (!kFp8) {
+          const uint32_t ph0 = pack_bf16x2(pr[0], pr[1]);
+          const uint32_t ph1 = pack_bf16x2(pr[2], pr[3]);
+          const uint32_t pl0 =
+              pack_bf16x2(pr[0] - bf16lo_to_f32(ph0), pr[1] - bf16hi_to_f32(ph0));
+          const uint32_t pl1 =
+              pack_bf16x2(pr[2] - bf16lo_to_f32(ph1), pr[3] - bf16hi_to_f32(ph1));
+          const int vrow = ((lane >> 4) << 3) + (lane & 7);  // key row of this lane's address
+#pragma unroll
+          for (int j = 0; j < C::kKSteps; ++j) {
+            const int chunk = 2 * j + ((lane >> 3) & 1);
+            const uint32_t addr = vbase + (chunk >> 3) * C::kBoxBytes + vrow * 128 +
+                                  (((chunk & 7) ^ (vrow & 7)) << 4);
+            uint32_t a[4];
+            ldsm_x4_t(addr, a[0], a[1], a[2], a[3]);
+            a[0] &= vm_lo;
+            a[1] &= vm_lo;
+            a[2] &= vm_hi;
+            a[3] &= vm_hi;
+            mma_bf16(oacc[j], a, ph0, ph1);
+            mma_bf16(oacc[j], a, pl0, pl1);
+          }
+        } else {
+          const uint32_t pf0 = pack_f16x2(pr[0], pr[1]);
+          const uint32_t pf1 = pack_f16x2(pr[2], pr[3]);
+          const int vrow = ((lane >> 3) & 1) * 8 + (lane & 7);
+#pragma unroll
+          for (int jj = 0; jj < D / 32; ++jj) {
+            const int chunk = 2 * jj + (lane >> 4);
+            const uint32_t addr = vbase + vrow * 128 + (((chunk & 7) ^ (vrow & 7)) << 4);
+            uint32_t r[4];  // (keys 0-7, chunk 2jj), (8-15, 2jj), (0-7, 2jj+1), (8-15, 2jj+1)
+            ldsm_x4_t(addr, r[0], r[1], r[2], r[3]);
+            r[0] &= vm_lo;
+            r[1] &= vm_hi;
+            r[2] &= vm_lo;
+            r[3] &= vm_hi;
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const uint32_t lo = r[2 * h2], hi = r[2 * h2 + 1];
+              const uint32_t a[4] = {
+                  e4m3x2_to_f16x2(static_cast<uint16_t>(prmt(lo, 0u, 0x0020u))),
+                  e4m3x2_to_f16x2(static_cast<uint16_t>(prmt(lo, 0u, 0x0031u))),
+                  e4m3x2_to_f16x2(static_cast<uint16_t>(prmt(hi, 0u, 0x0020u))),
+                  e4m3x2_to_f16x2(static_cast<uint16_t>(prmt(hi, 0u, 0x0031u)))};
+              mma_f16(oacc[2 * jj + h2], a, pf0, pf1);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      ++it;
+      if (k + NST < nb_w) issue(k + NST);
+    }
+    if (timed_out) it = 0;  // results are void; phase tracking no longer matters
+
+    // ---- per-warp state -> shared memory (this warp's own stage buffers) -----------------
+    float l_row = l_run;
+    l_row += __shfl_xor_sync(0xffffffffu, l_row, 1);
+    l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
+    float* so = reinterpret_cast<float*>(wbuf);           // [8][D]
+    float* sm = so + kRowsPerTile * D;                     // [8]
+    float* sl = sm + kRowsPerTile;                         // [8]
+#pragma unroll
+    for (int j = 0; j < C::kKSteps; ++j) {
+      int da, db;
+      if constexpr (!kFp8) {
+        da = 16 * j + quad;
+        db = da + 8;
+      } else {
+        da = 16 * j + 2 * quad;
+        db = da + 1;
+      }
+      so[(2 * qc) * D + da] = oacc[j][0];
+      so[(2 * qc + 1) * D + da] = oacc[j][1];
+      so[(2 * qc) * D + db] = oacc[j][2];
+      so[(2 * qc + 1) * D + db] = oacc[j][3];
+    }
+    if (qc == 0) {
+      sm[quad] = m_run;
+      sl[quad] = l_row;
+    }
+    __syncthreads();
+
+    // ---- merge the 4 warps and write the output or the partial ---------------------------
+    for (int e = threadIdx.x; e < I.rows * D; e += kDecodeWarps * 32) {
+      const int r = e / D, d = e - r * D;
+      float M = -CUDART_INF_F;
+#pragma unroll
+      for (int w = 0; w < kDecodeWarps; ++w) {
+        const float* wsm = reinterpret_cast<const float*>(smem + w * NST * C::kStageBytes) +
+                           kRowsPerTile * D;
+        M = fmaxf(M, wsm[r]);
+      }
+      float Lsum = 0.f, O = 0.f;
+      if (M != -CUDART_INF_F) {
+#pragma unroll
+        for (int w = 0; w < kDecodeWarps; ++w) {
+          const float* wso = reinterpret_cast<const float*>(smem + w * NST * C::kStageBytes);
+          const float mw = wso[kRowsPerTile * D + r];
+          const float f = fast_exp2(mw - M);
+          Lsum += wso[kRowsPerTile * D + kRowsPerTile + r] * f;
+          O += wso[r * D + d] * f;
+        }
+      }
+      const float val = Lsum > 0.f ? O / Lsum * p.v_out_scale : 0.f;
+      const int t = I.t0 + r / p.group;
+      const int hq = I.h * p.group + r % p.group;
+      const int64_t orow = static_cast<int64_t>(t) * p.num_q_heads + hq;
+      if (I.nparts == 1) {
+        if (p.out_bf16)
+          reinterpret_cast<__nv_bfloat16*>(p.out)[orow * D + d] = __float2bfloat16_rn(val);
+        else
+          reinterpret_cast<float*>(p.out)[orow * D + d] = val;
+      } else {
+        const int64_t prow = orow * p.pmax + I.part;
+        p.part_o[prow * D + d] = val;
+        if (d == 0) p.part_lse[prow] = Lsum > 0.f ? M + __log2f(Lsum) : -CUDART_INF_F;
+      }
+    }
+    __syncthreads();
+    fence_proxy_async_smem();  // generic accesses to the stage buffers before the next TMA
+  }
+}
+
+// One warp per (token, q head) row of a sequence that was split into several partitions.
+template <int D>
+__global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p, int32_t num_tokens) {
+  const int lane = threadIdx.x & 31;
+  const int64_t rid = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (rid >= static_cast<int64_t>(num_tokens) * p.num_q_heads) return;
+  const int t = static_cast<int>(rid / p.num_q_heads);
+  int lo = 0, hi = p.num_seqs;  // sequence of token t: largest s with qsl[s] <= t
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (p.qsl[mid] <= t) lo = mid; else hi = mid;
+  }
+  const int s = lo;
+  const int n = p.qsl[s + 1] - p.qsl[s];
+  const int L = p.context_lens[s];
+  bool bad;
+  if (decode_items_of(p, n, L, &bad) == 0) return;  // prefill path, invalid, or empty
+  const int nparts = ceil_div(ceil_div(L, kBlockSize), p.pblk);
+  if (nparts <= 1) return;
+  const float* lse = p.part_lse + rid * p.pmax;
+  float M = -CUDART_INF_F;
+  for (int i = lane; i < nparts; i += 32) M = fmaxf(M, lse[i]);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  constexpr int kPer = D / 32;
+  float acc[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
+  float wsum = 0.f;
+  const float* po = p.part_o + rid * p.pmax * D;
+  for (int base = 0; base < nparts; base += 32) {
+    const int i = base + lane;
+    const float w = (i < nparts && M != -CUDART_INF_F) ? fast_exp2(lse[i] - M) : 0.f;
+    const int cnt = min(32, nparts - base);
+    for (int j = 0; j < cnt; ++j) {
+      const float wj = __shfl_sync(0xffffffffu, w, j);
+      wsum += wj;
+      if (wj != 0.f) {
+        const float* src = po + static_cast<int64_t>(base + j) * D + lane * kPer;
+        if constexpr (kPer == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(src);
+          acc[0] += wj * v.x;
+          acc[1] += wj * v.y;
+          acc[2] += wj * v.z;
+          acc[3] += wj * v.w;
+        } else {
+#pragma unroll
+          for (int i2 = 0; i2 < kPer; ++i2) acc[i2] += wj * src[i2];
+        }
+      }
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int64_t o = rid * D + lane * kPer + i;
+    if (p.out_bf16)
+      reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(acc[i] * inv);
+    else
+      reinterpret_cast<float*>(p.out)[o] = acc[i] * inv;
+  }
+}
+
+template <int D, bool kFp8, int NST>
+static cudaError_t run_decode(const AttnArgs& a, const WsLayout& ws, const DecodeParams& p,
+                              const CUtensorMap& kmap, const CUtensorMap& vmap,
+                              cudaEvent_t before, cudaEvent_t after) {
+  constexpr int smem = decode_smem_bytes<D, kFp8, NST>();
+  auto kern = decode_kernel<D, kFp8, NST>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecodeWarps * 32, smem);
+  if (per_sm < 1) per_sm = 1;
+  const int tpt = kRowsPerTile / p.group;
+  const int64_t qtiles_max =
+      (std::min(a.max_query_len, ws.decode_max_query) + tpt - 1) / tpt;
+  const int64_t upper = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads * qtiles_max * ws.pmax;
+  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(upper, int64_t(sms) * per_sm));
+  if (before) cudaEventRecord(before, a.stream);
+  kern<<<static_cast<unsigned>(grid), kDecodeWarps * 32, smem, a.stream>>>(kmap, vmap, p);
+  if (after) cudaEventRecord(after, a.stream);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (ws.pmax > 1) {
+    const int64_t rows = static_cast<int64_t>(a.num_q_tokens) * a.num_q_heads;
+    const int64_t blocks = (rows + 7) / 8;
+    if (blocks > 0)
+      merge_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, a.stream>>>(p, a.num_q_tokens);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const CUtensorMap& kmap,
+                             const CUtensorMap& vmap, cudaEvent_t before, cudaEvent_t after) {
+  uint8_t* wsb = static_cast<uint8_t*>(a.workspace);
+  DecodeParams p{};
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.block_tables = a.block_tables;
+  p.context_lens = a.context_lens;
+  p.qsl = a.query_start_loc;
+  p.item_start = reinterpret_cast<int32_t*>(wsb + ws.item_start);
+  p.part_lse = reinterpret_cast<float*>(wsb + ws.part_lse);
+  p.part_o = reinterpret_cast<float*>(wsb + ws.part_o);
+  p.out = a.out;
+  p.hdr = reinterpret_cast<WsHeader*>(wsb);
+  p.max_blocks_per_seq = a.max_blocks_per_seq;
+  p.num_seqs = a.num_seqs;
+  p.num_q_heads = a.num_q_heads;
+  p.num_kv_heads = a.num_kv_heads;
+  p.group = a.num_q_heads / a.num_kv_heads;
+  p.num_blocks = a.cache.num_blocks;
+  p.max_context_len = a.max_context_len;
+  p.max_query_len = a.max_query_len;
+  p.pblk = ws.pblk;
+  p.pmax = ws.pmax;
+  p.decode_max_query = ws.decode_max_query;
+  p.out_bf16 = a.out_dtype == PA_BF16;
+  const float log2e = 1.4426950408889634f;
+  const bool fp8 = a.cache.cache_dtype == PA_FP8_E4M3;
+  p.score_log2 = a.scale * log2e * (fp8 ? a.cache.k_scale : 1.f);
+  p.v_out_scale = fp8 ? a.cache.v_scale : 1.f;
+
+  plan_kernel<<<1, 1024, 0, a.stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (fp8) return run_decode<128, true, 4>(a, ws, p, kmap, vmap, before, after);
+  if (a.head_dim == 128) return run_decode<128, false, 3>(a, ws, p, kmap, vmap, before, after);
+  return run_decode<64, false, 4>(a, ws, p, kmap, vmap, before, after);
+}
+
+}  // namespace pa

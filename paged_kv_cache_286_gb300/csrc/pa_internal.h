@@ -1,0 +1,60 @@
+// Host-side interfaces between the C-ABI layer (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa {
+
+// Everything pa_attention received, after host validation.
+struct AttnArgs {
+  const void* q;
+  int32_t num_q_tokens;
+  const void* k_cache;
+  const void* v_cache;
+  pa_cache_desc cache;
+  const int32_t* block_tables;
+  int32_t max_blocks_per_seq;
+  const int32_t* context_lens;
+  const int32_t* query_start_loc;
+  int32_t num_seqs;
+  int32_t max_context_len;
+  int32_t max_query_len;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  float scale;
+  void* out;
+  int32_t out_dtype;
+  void* workspace;
+  size_t workspace_bytes;
+  cudaStream_t stream;
+};
+
+// Workspace carve-up; a pure function of the step's shape (see workspace_layout).
+struct WsLayout {
+  size_t item_start;  // int32 [num_seqs + 1], decode work-item prefix sums
+  size_t part_lse;    // float [num_q_tokens][num_q_heads][pmax], log2-domain log-sum-exp
+  size_t part_o;      // float [num_q_tokens][num_q_heads][pmax][head_dim], normalised partials
+  size_t total;
+  int32_t pblk;       // blocks per KV partition
+  int32_t pmax;       // partitions per sequence at most
+  int32_t decode_max_query;  // sequences with more queries go to the prefill path
+};
+
+WsLayout workspace_layout(int32_t num_seqs, int32_t num_q_tokens, int32_t num_q_heads,
+                          int32_t num_kv_heads, int32_t head_dim, int32_t max_context_len,
+                          int32_t max_query_len);
+
+cudaError_t launch_cache_append(const void* k, const void* v, const int64_t* slots,
+                                int32_t num_tokens, void* k_cache, void* v_cache,
+                                const pa_cache_desc& c, uint32_t* err, cudaStream_t stream);
+
+cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const CUtensorMap& kmap,
+                             const CUtensorMap& vmap, cudaEvent_t before, cudaEvent_t after);
+
+}  // namespace pa

@@ -1,0 +1,253 @@
+"""Parity of the CUDA library (through its C ABI) with the fp64 oracle.
+
+Append: bit-exact against the oracle's scatter, for bf16 and E4M3 pools, untouched slots
+included.  Attention: max |gpu - oracle| <= 2e-3 for bf16 K/V and 2e-2 for E4M3 K/V (fp32
+output), element by element, on cases that span several partitions and a ragged last block, on
+the five named workloads (all rows of the tiny one; sampled sequences of the full-size ones,
+in the same launch configuration the benchmark times), and on edge cases.  GPU invariants:
+permuting the physical blocks and sharing vs duplicating a prefix give bitwise-identical output.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+from oracle import cache_append, e4m3_encode_f32, paged_attention, run_step  # noqa: E402
+from synthetic import make_config, make_workload  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_kv_cache_286_gb300 import build
+    build.build()
+
+
+def _h():
+    import gpu_harness
+    return gpu_harness
+
+
+def _oracle_pools(w):
+    kp, vp = cache_append(w.empty_pool(), w.empty_pool(), w.k_prior_bits, w.v_prior_bits,
+                          w.slot_prior, w.block_size, w.cache_dtype, w.k_scale, w.v_scale)
+    return cache_append(kp, vp, w.k_new_bits, w.v_new_bits, w.slot_mapping, w.block_size,
+                        w.cache_dtype, w.k_scale, w.v_scale)
+
+
+def _check_small(w, out_dtype=torch.float32):
+    h = _h()
+    d, out = h.run_gpu(w, out_dtype)
+    kp, vp, ref = run_step(w)
+    gk, gv = d.pools_numpy()
+    assert np.array_equal(gk, kp) and np.array_equal(gv, vp), "append is not bit-exact"
+    return h.assert_close_to_oracle(w, out, ref)
+
+
+# ---- the tiny named workload, every row ----------------------------------------------------
+def test_config1_all_rows():
+    _check_small(make_config(1))
+
+
+@pytest.mark.parametrize("fill", ["zero", "nan"])
+def test_config1_stale_slots_do_not_leak(fill):
+    """Unwritten slots of a sequence's last block hold NaN patterns; they must be masked."""
+    _check_small(make_config(1, pool_fill=fill))
+
+
+# ---- small cases spanning partitions and ragged tails ------------------------------------
+EDGE_CTX = [1, 15, 16, 17, 32, 33, 100, 511, 512, 513, 2000]
+
+
+@pytest.mark.parametrize("hq,hkv,d,dtype", [
+    (4, 4, 128, "bf16"), (8, 4, 128, "bf16"), (16, 4, 128, "bf16"), (32, 4, 128, "bf16"),
+    (4, 4, 64, "bf16"), (16, 2, 64, "bf16"),
+    (8, 8, 128, "fp8_e4m3"), (16, 4, 128, "fp8_e4m3"), (32, 4, 128, "fp8_e4m3"),
+])
+def test_decode_edge_lengths(hq, hkv, d, dtype):
+    w = make_workload(EDGE_CTX, [1] * len(EDGE_CTX), num_q_heads=hq, num_kv_heads=hkv,
+                      head_dim=d, cache_dtype=dtype, seed=hq * 131 + d, pool_fill="nan",
+                      extra_table_cols=3)
+    _check_small(w)
+
+
+@pytest.mark.parametrize("qlens,ctx", [
+    ([2, 3, 7, 16], [40, 3, 200, 16]),            # short multi-query runs (speculative verify)
+    ([37, 1, 64], [37, 900, 300]),                # chunk with no prior context; chunk on prefix
+    ([0, 5, 0, 1], [10, 70, 33, 1]),              # sequences with nothing to do
+])
+@pytest.mark.parametrize("dtype", ["bf16", "fp8_e4m3"])
+def test_multi_query_causal(qlens, ctx, dtype):
+    w = make_workload(ctx, qlens, num_q_heads=16, num_kv_heads=4, head_dim=128,
+                      cache_dtype=dtype, seed=sum(ctx), pool_fill="nan")
+    _check_small(w)
+
+
+def test_single_sequence_long_context_splits():
+    w = make_workload([9000], [1], num_q_heads=8, num_kv_heads=2, head_dim=128, seed=5)
+    _check_small(w)
+
+
+def test_bf16_output():
+    w = make_workload(EDGE_CTX, [1] * len(EDGE_CTX), num_q_heads=8, num_kv_heads=2,
+                      head_dim=128, seed=77)
+    _check_small(w, out_dtype=torch.bfloat16)
+
+
+# ---- append -------------------------------------------------------------------------------
+def test_append_skips_negative_slots():
+    h = _h()
+    w = make_workload([50, 20], [50, 20], num_q_heads=4, num_kv_heads=4, head_dim=64, seed=8)
+    w.slot_mapping = w.slot_mapping.copy()
+    w.slot_mapping[::3] = -1
+    d = h.DeviceStep(w)
+    d.append_new()
+    assert __import__("paged_kv_cache_286_gb300").check_error(d.ws) == 0
+    kp, vp = cache_append(w.empty_pool(), w.empty_pool(), w.k_new_bits, w.v_new_bits,
+                          w.slot_mapping, 16)
+    gk, gv = d.pools_numpy()
+    assert np.array_equal(gk, kp) and np.array_equal(gv, vp)
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.012904576, 3.7, 2.0 ** -20])
+def test_e4m3_append_every_bf16_value(scale):
+    """Every one of the 65536 bf16 bit patterns quantised on append equals the oracle's OCP
+    encoding of fl32(x) / scale (round to nearest even, saturating; NaN -> 0x7F)."""
+    import paged_kv_cache_286_gb300 as pa
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(512, 1, 128)
+    slots = np.arange(512, dtype=np.int64)
+    k = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+    kc = torch.zeros((32, 1, 16, 128), dtype=torch.uint8, device="cuda")
+    vc = torch.zeros_like(kc)
+    ws = pa.new_workspace(256)
+    pa.cache_append(k, k, torch.from_numpy(slots).cuda(), kc, vc, ws, k_scale=scale,
+                    v_scale=scale)
+    assert pa.check_error(ws) == 0
+    got = kc.cpu().numpy()[slots // 16, 0, slots % 16, :]
+    x = (bits.astype(np.uint32) << 16).view(np.float32)[:, 0, :]
+    want = e4m3_encode_f32(np.divide(x, np.float32(scale), dtype=np.float32))
+    nan_in = np.isnan(x)
+    assert np.array_equal(got[~nan_in], want[~nan_in])
+    assert np.all((got[nan_in] & 0x7F) == 0x7F)        # NaN stays NaN
+
+
+# ---- invariants on the GPU ---------------------------------------------------------------
+def test_block_permutation_is_bitwise_invariant():
+    h = _h()
+    w = make_workload([300, 1000, 17, 4000], [1, 1, 1, 1], num_q_heads=16, num_kv_heads=4,
+                      head_dim=128, seed=9, pool_factor=1.5)
+    d1, out1 = h.run_gpu(w)
+    out1 = out1.clone()
+    perm = np.random.default_rng(1).permutation(w.num_blocks)
+    w2 = make_workload([300, 1000, 17, 4000], [1, 1, 1, 1], num_q_heads=16, num_kv_heads=4,
+                       head_dim=128, seed=9, pool_factor=1.5)
+    w2.block_tables = np.where(w.block_tables >= 0, perm[np.maximum(w.block_tables, 0)], -1) \
+        .astype(np.int32)
+    w2.slot_mapping = perm[w.slot_mapping // 16] * 16 + w.slot_mapping % 16
+    w2.slot_prior = perm[w.slot_prior // 16] * 16 + w.slot_prior % 16
+    d2, out2 = h.run_gpu(w2)
+    assert torch.equal(out1, out2)
+
+
+def test_shared_prefix_equals_duplicated_prefix_bitwise():
+    h = _h()
+    ctx = [2000, 1700, 1300]
+    w = make_workload(ctx, [1, 1, 1], num_q_heads=8, num_kv_heads=2, head_dim=128, seed=10,
+                      shared_prefix_blocks=20, pool_factor=2.0)
+    d, out_shared = h.run_gpu(w)
+    out_shared = out_shared.clone()
+    # duplicate the 20 shared blocks into private copies for sequences 1 and 2
+    used = set(w.block_tables[w.block_tables >= 0].tolist())
+    free = [b for b in range(w.num_blocks) if b not in used]
+    tables = w.block_tables.copy()
+    for s in (1, 2):
+        for j in range(20):
+            b = free.pop()
+            d.k_cache[b] = d.k_cache[tables[s, j]]
+            d.v_cache[b] = d.v_cache[tables[s, j]]
+            tables[s, j] = b
+    assert len(set(tables[:, :20].ravel().tolist())) == 60
+    d.tables = torch.from_numpy(tables).cuda()
+    out_dup = d.attend()
+    assert torch.equal(out_shared, out_dup)
+
+
+# ---- device-side errors (bounds checks; nothing is read out of bounds) -------------------
+def test_out_of_range_block_id_sets_error_word():
+    import paged_kv_cache_286_gb300 as pa
+    h = _h()
+    w = make_workload([100, 50], [1, 1], num_q_heads=4, num_kv_heads=4, head_dim=64, seed=3)
+    d = h.DeviceStep(w)
+    d.append_prior()
+    d.append_new()
+    bad = w.block_tables.copy()
+    bad[0, 2] = w.num_blocks + 5
+    bad[1, 0] = -7
+    d.tables = torch.from_numpy(bad).cuda()
+    d.attend()
+    word = pa.check_error(d.ws, raise_on_error=False)
+    assert word & pa._lib.PA_DEVERR_BLOCK_ID
+    assert pa.check_error(d.ws) == 0        # reading clears it
+
+
+def test_out_of_range_slot_sets_error_word():
+    import paged_kv_cache_286_gb300 as pa
+    h = _h()
+    w = make_workload([10], [10], num_q_heads=4, num_kv_heads=4, head_dim=64, seed=4)
+    d = h.DeviceStep(w)
+    d.slots[3] = w.num_blocks * 16
+    d.append_new()
+    with pytest.raises(pa.PagedAttnError):
+        pa.check_error(d.ws)
+
+
+def test_inconsistent_lengths_set_error_word():
+    import paged_kv_cache_286_gb300 as pa
+    h = _h()
+    w = make_workload([10, 40], [1, 1], num_q_heads=4, num_kv_heads=4, head_dim=64, seed=6)
+    d = h.DeviceStep(w)
+    d.append_prior()
+    d.append_new()
+    d.ctx[0] = 0                      # n_s = 1 > context_len = 0
+    d.attend()
+    word = pa.check_error(d.ws, raise_on_error=False)
+    assert word & pa._lib.PA_DEVERR_LENGTHS
+
+
+# ---- the full-size named workloads (launch configuration of the benchmark) ---------------
+def _sampled(cid, n_seq, extra=()):
+    h = _h()
+    w = make_config(cid)
+    d, out = h.run_gpu(w)
+    kp, vp = _oracle_pools(w)
+    gk, gv = d.pools_numpy()
+    assert np.array_equal(gk, kp) and np.array_equal(gv, vp), "append is not bit-exact"
+    del gk, gv
+    rng = np.random.default_rng(cid)
+    seqs = sorted(set(rng.choice(w.num_seqs, size=min(n_seq, w.num_seqs), replace=False)
+                      .tolist()) | set(extra))
+    ref = paged_attention(w.q_bits, kp, vp, w.block_tables, w.context_lens, w.query_start_loc,
+                          w.num_q_heads, w.num_kv_heads, w.head_dim, w.scale, w.block_size,
+                          w.cache_dtype, w.k_scale, w.v_scale, seqs=seqs)
+    return h.assert_close_to_oracle(w, out, ref)
+
+
+@pytest.mark.slow
+def test_config2_full_size_sampled():
+    _sampled(2, 8)
+
+
+@pytest.mark.slow
+def test_config3_full_size_sampled():
+    _sampled(3, 16, extra=[int(np.argmax(make_config(3).context_lens))])
+
+
+@pytest.mark.slow
+def test_config4_full_size_sampled():
+    _sampled(4, 6, extra=[48, 49])          # both prefill chunks
+
+
+@pytest.mark.slow
+def test_config5_full_size_sampled():
+    _sampled(5, 2)
