@@ -51,6 +51,9 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seqs", type=int, default=0,
+                    help="keep only the first N sequences of the workload (small profiling "
+                         "cases; 0 = all)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="budget of the oracle CPU-baseline sample")
@@ -353,7 +356,13 @@ def run_ours(args):
     import paged_kv_cache_286_gb300 as pa
     from synthetic.workloads import CONFIG_NAMES, make_config
 
-    w = make_config(args.config)
+    if args.seqs:
+        from synthetic.workloads import config_lengths, make_workload
+        ctx, ql, kw = config_lengths(args.config)
+        w = make_workload(ctx[:args.seqs], ql[:args.seqs], seed=1000 + args.config,
+                          name=f"cfg{args.config}-first{args.seqs}", **kw)
+    else:
+        w = make_config(args.config)
     dw = DeviceWorkload(w, device)
     algo_attn = w.algorithmic_bytes()
     algo_step = algo_attn + w.append_bytes()
@@ -421,7 +430,8 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3" if w.cache_dtype == "fp8_e4m3" else "bf16", "data": "synthetic",
-            "config": {"workload": f"cfg{args.config}: {CONFIG_NAMES[args.config]}",
+            "config": {"workload": f"cfg{args.config}: {CONFIG_NAMES[args.config]}"
+                                   + (f" (first {args.seqs} sequences)" if args.seqs else ""),
                        "l2": f"no flush: each step streams {algo_attn / 1e9:.2f} GB of K/V "
                              "and q/out, far above the 129 MB L2",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
