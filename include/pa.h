@@ -138,6 +138,35 @@ pa_status pa_attention(const void* q, int32_t num_q_tokens, const void* k_cache,
                        void* out, int32_t out_dtype, void* workspace, size_t workspace_bytes,
                        cudaStream_t stream);
 
+/* Scratch bytes built into the library for pa_attention_noalloc (32 MiB per device). */
+#define PA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/* pa_attention for callers that cannot allocate device memory.  (The pages have no
+ * counterpart: this is a library convenience, not part of the method.)
+ *
+ * Some callers are not allowed to call cudaMalloc: code running under a memory manager that
+ * owns all device memory, code that must not grow its footprint after start-up, or code on a
+ * path where an allocation could stall the device.  They can still pass inputs and outputs but
+ * not a workspace, so this call uses a scratch array built into the library instead:
+ * PA_NOALLOC_SCRATCH_BYTES per device, held by every GPU that loads the library until the
+ * process exits.  A step whose pa_attention_workspace_size exceeds it is rejected with
+ * PA_ERR_INVALID_ARG and a message; use pa_attention with a workspace for larger steps.
+ *   Arguments are those of pa_attention without workspace/workspace_bytes, plus
+ *   error_word    optional DEVICE pointer (may be NULL) that receives, asynchronously on
+ *                 `stream`, this call's PA_DEVERR_* bits.
+ * The first call on a device looks up the scratch array's device address (once per device, with
+ * that device current); make that first call before any stream capture.  Every call shares the
+ * one array and overwrites it, starting from a cleared header: calls whose GPU work overlaps
+ * (other streams, other threads) race on it and must be serialised by the caller. */
+pa_status pa_attention_noalloc(const void* q, int32_t num_q_tokens, const void* k_cache,
+                               const void* v_cache, const pa_cache_desc* cache,
+                               const int32_t* block_tables, int32_t max_blocks_per_seq,
+                               const int32_t* context_lens, const int32_t* query_start_loc,
+                               int32_t num_seqs, int32_t max_context_len, int32_t max_query_len,
+                               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                               float scale, void* out, int32_t out_dtype, uint32_t* error_word,
+                               cudaStream_t stream);
+
 /* Synchronise `stream`, read and clear the device error word at the start of `workspace`.
  * Returns PA_OK, PA_ERR_OUT_OF_RANGE (block id / slot / length bits), PA_ERR_TIMEOUT, or
  * PA_ERR_CUDA.  *word_out (may be NULL) receives the raw PA_DEVERR_* bits. */

@@ -12,6 +12,7 @@ PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_OUT_OF_RANGE, PA_ERR_TIMEO
     PA_ERR_CUDA = range(6)
 PA_BF16, PA_FP8_E4M3, PA_FP32 = 0, 1, 2
 PA_WORKSPACE_HEADER_BYTES = 256
+PA_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 PA_DEVERR_BLOCK_ID, PA_DEVERR_SLOT, PA_DEVERR_LENGTHS, PA_DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 
 STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED",
@@ -19,7 +20,7 @@ STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED",
 
 EXPORTED = ["pa_cache_append", "pa_attention_workspace_size", "pa_attention", "pa_check_error",
             "pa_workspace_init", "pa_last_error_string", "pa_version",
-            "pa_set_kernel_timing_events"]
+            "pa_set_kernel_timing_events", "pa_attention_noalloc"]
 
 
 class CacheDesc(ctypes.Structure):
@@ -57,6 +58,10 @@ def load() -> ctypes.CDLL:
                                i32, i32, i32, i32, i32, i32, ctypes.c_float, vp, i32, vp,
                                ctypes.c_size_t, vp]
     L.pa_attention.restype = ctypes.c_int
+    L.pa_attention_noalloc.argtypes = [vp, i32, vp, vp, ctypes.POINTER(CacheDesc), i32p, i32,
+                                       i32p, i32p, i32, i32, i32, i32, i32, i32, ctypes.c_float,
+                                       vp, i32, vp, vp]
+    L.pa_attention_noalloc.restype = ctypes.c_int
     L.pa_check_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
     L.pa_check_error.restype = ctypes.c_int
     L.pa_workspace_init.argtypes = [vp, vp]

@@ -135,6 +135,10 @@ WsLayout workspace_layout(int32_t S, int32_t T, int32_t Hq, int32_t Hkv, int32_t
   return w;
 }
 
+// Lets other translation units of the library report a host-side error through
+// pa_last_error_string.
+void set_last_error(const char* msg) { g_last_error = msg; }
+
 }  // namespace pa
 
 extern "C" {

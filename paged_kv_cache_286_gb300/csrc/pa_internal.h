@@ -54,6 +54,8 @@ cudaError_t launch_cache_append(const void* k, const void* v, const int64_t* slo
                                 int32_t num_tokens, void* k_cache, void* v_cache,
                                 const pa_cache_desc& c, uint32_t* err, cudaStream_t stream);
 
+void set_last_error(const char* msg);
+
 cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, cudaEvent_t before, cudaEvent_t after);
 
