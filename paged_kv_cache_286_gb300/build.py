@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpagedattn.so")
-SOURCES = ["api.cu", "append.cu", "decode.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "append.cu", "decode.cu", "noalloc.cu", "prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -70,6 +70,25 @@ pa_status encode_pool_map(CUtensorMap* map, const void* base, const pa_cache_des
   return PA_OK;
 }
 
+// 3-D view of q [T][Hq][D] bf16; one box = (64 columns, G heads, 128 / G tokens) = 128 rows
+// of 128 bytes with the 128-byte swizzle, the q tile of one prefill work item.
+pa_status encode_q_map(CUtensorMap* map, const void* q, int32_t T, int32_t Hq, int32_t D,
+                       int32_t G) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq),
+                              static_cast<cuuint64_t>(T)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(Hq) * D * 2};
+  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(128 / G)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled (q) failed (%d)", int(r));
+  return PA_OK;
+}
+
 pa_status check_cache_desc(const pa_cache_desc* c, bool for_attention) {
   if (!c) return fail(PA_ERR_INVALID_ARG, "cache descriptor is NULL");
   if (c->num_blocks <= 0 || c->num_kv_heads <= 0 || c->head_dim <= 0 || c->block_size <= 0)
@@ -105,9 +124,10 @@ WsLayout workspace_layout(int32_t S, int32_t T, int32_t Hq, int32_t Hkv, int32_t
                           int32_t max_ctx, int32_t max_q) {
   WsLayout w{};
   const int32_t G = Hkv > 0 ? Hq / Hkv : 1;
-  w.decode_max_query = INT32_MAX;  // every sequence takes the split-KV path
+  // the partition size depends only on the shape (not on the cache dtype): sized as if chunks
+  // longer than kDecodeMaxQuery queries go to the prefill path
   const int64_t tpt = std::max(1, kRowsPerTile / std::max(1, G));
-  const int64_t qtiles = (std::max<int64_t>(1, std::min(max_q, w.decode_max_query)) + tpt - 1) / tpt;
+  const int64_t qtiles = (std::max<int64_t>(1, std::min(max_q, kDecodeMaxQuery)) + tpt - 1) / tpt;
   const int64_t maxblk = (std::max(1, max_ctx) + kBlockSize - 1) / kBlockSize;
   // Largest partition that still yields enough work items to fill the GPU; a partition never
   // has fewer than 8 blocks (2 per warp).
@@ -124,6 +144,8 @@ WsLayout workspace_layout(int32_t S, int32_t T, int32_t Hq, int32_t Hkv, int32_t
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   size_t off = PA_WORKSPACE_HEADER_BYTES;
   w.item_start = off;
+  off = up(off + sizeof(int32_t) * (size_t(std::max(S, 0)) + 1));
+  w.pf_item_start = off;
   off = up(off + sizeof(int32_t) * (size_t(std::max(S, 0)) + 1));
   const size_t rows = size_t(std::max(T, 0)) * size_t(std::max(Hq, 0));
   const size_t parts = w.pmax > 1 ? size_t(w.pmax) : 0;
@@ -252,11 +274,20 @@ pa_status pa_attention(const void* q, int32_t num_q_tokens, const void* k_cache,
   if ((st = encode_pool_map(&kmap, k_cache, *cache)) != PA_OK) return st;
   if ((st = encode_pool_map(&vmap, v_cache, *cache)) != PA_OK) return st;
 
+  CUtensorMap qmap;
+  const bool use_prefill = pa::prefill_path_enabled(*cache, num_q_heads, num_kv_heads) &&
+                           max_query_len > pa::kDecodeMaxQuery;
+  if (use_prefill &&
+      (st = encode_q_map(&qmap, q, num_q_tokens, num_q_heads, head_dim,
+                         num_q_heads / num_kv_heads)) != PA_OK)
+    return st;
+
   pa::AttnArgs a{q, num_q_tokens, k_cache, v_cache, *cache, block_tables, max_blocks_per_seq,
                  context_lens, query_start_loc, num_seqs, max_context_len, max_query_len,
                  num_q_heads, num_kv_heads, head_dim, scale, out, out_dtype, workspace,
                  workspace_bytes, stream};
-  cudaError_t e = pa::launch_attention(a, ws, kmap, vmap, g_before, g_after);
+  cudaError_t e =
+      pa::launch_attention(a, ws, kmap, vmap, use_prefill ? &qmap : nullptr, g_before, g_after);
   if (e != cudaSuccess) return cuda_fail(e, "pa_attention launch");
   return PA_OK;
 }

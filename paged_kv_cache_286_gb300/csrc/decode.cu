@@ -37,6 +37,7 @@ struct DecodeParams {
   const int32_t* context_lens;
   const int32_t* qsl;
   int32_t* item_start;
+  int32_t* pf_item_start;
   float* part_lse;
   float* part_o;
   void* out;
@@ -78,51 +79,76 @@ __device__ __forceinline__ int decode_items_of(const DecodeParams& p, int n, int
   return p.num_kv_heads * qtiles * nparts;
 }
 
-// One CTA: exclusive prefix sum of decode items over sequences; resets the work counters.
+// Prefill-path items of one sequence: one per (kv head, 128-row tile of tokens x heads).
+__device__ __forceinline__ int prefill_items_of(const DecodeParams& p, int n, int L) {
+  bool bad;
+  if (decode_items_of(p, n, L, &bad) != 0 || bad || n <= p.decode_max_query) return 0;
+  const int tpt = 128 / p.group;
+  return p.num_kv_heads * ceil_div(n, tpt);
+}
+
+// One CTA: exclusive prefix sums of decode and prefill items over sequences; resets the work
+// counters and flags inconsistent lengths.
 __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
-  __shared__ int warp_sums[32];
-  __shared__ int carry_s;
+  __shared__ int2 warp_sums[32];
+  __shared__ int2 carry_s;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) carry_s = 0;
+  if (tid == 0) carry_s = make_int2(0, 0);
   __syncthreads();
   for (int base = 0; base < p.num_seqs; base += 1024) {
     const int s = base + tid;
-    int cnt = 0;
+    int2 cnt = make_int2(0, 0);
     if (s < p.num_seqs) {
       const int n = p.qsl[s + 1] - p.qsl[s];
       const int L = p.context_lens[s];
       bool bad;
-      cnt = decode_items_of(p, n, L, &bad);
+      cnt.x = decode_items_of(p, n, L, &bad);
       if (bad) set_error(&p.hdr->error, PA_DEVERR_LENGTHS);
+      cnt.y = prefill_items_of(p, n, L);
     }
-    int x = cnt;  // inclusive warp scan
+    int2 x = cnt;  // inclusive warp scan of both counts
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
+      const int yx = __shfl_up_sync(0xffffffffu, x.x, o);
+      const int yy = __shfl_up_sync(0xffffffffu, x.y, o);
+      if (lane >= o) {
+        x.x += yx;
+        x.y += yy;
+      }
     }
     if (lane == 31) warp_sums[warp] = x;
     __syncthreads();
     if (warp == 0) {
-      int w = warp_sums[lane];
+      int2 w = warp_sums[lane];
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, w, o);
-        if (lane >= o) w += y;
+        const int yx = __shfl_up_sync(0xffffffffu, w.x, o);
+        const int yy = __shfl_up_sync(0xffffffffu, w.y, o);
+        if (lane >= o) {
+          w.x += yx;
+          w.y += yy;
+        }
       }
       warp_sums[lane] = w;  // inclusive over warps
     }
     __syncthreads();
-    const int carry = carry_s;
-    const int excl = carry + (warp ? warp_sums[warp - 1] : 0) + x - cnt;
-    if (s < p.num_seqs) p.item_start[s] = excl;
+    const int2 carry = carry_s;
+    const int2 before = warp ? warp_sums[warp - 1] : make_int2(0, 0);
+    const int2 excl = make_int2(carry.x + before.x + x.x - cnt.x,
+                                carry.y + before.y + x.y - cnt.y);
+    if (s < p.num_seqs) {
+      p.item_start[s] = excl.x;
+      p.pf_item_start[s] = excl.y;
+    }
     __syncthreads();
-    if (tid == 1023) carry_s = excl + cnt;
+    if (tid == 1023) carry_s = make_int2(excl.x + cnt.x, excl.y + cnt.y);
     __syncthreads();
   }
   if (tid == 0) {
-    p.item_start[p.num_seqs] = carry_s;
+    p.item_start[p.num_seqs] = carry_s.x;
+    p.pf_item_start[p.num_seqs] = carry_s.y;
     p.hdr->decode_counter = 0;
+    p.hdr->prefill_counter = 0;
   }
 }
 
@@ -616,8 +642,7 @@ static cudaError_t run_decode(const AttnArgs& a, const WsLayout& ws, const Decod
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecodeWarps * 32, smem);
   if (per_sm < 1) per_sm = 1;
   const int tpt = kRowsPerTile / p.group;
-  const int64_t qtiles_max =
-      (std::min(a.max_query_len, ws.decode_max_query) + tpt - 1) / tpt;
+  const int64_t qtiles_max = (std::min(a.max_query_len, p.decode_max_query) + tpt - 1) / tpt;
   const int64_t upper = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads * qtiles_max * ws.pmax;
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(upper, int64_t(sms) * per_sm));
   if (before) cudaEventRecord(before, a.stream);
@@ -635,8 +660,15 @@ static cudaError_t run_decode(const AttnArgs& a, const WsLayout& ws, const Decod
   return e;
 }
 
+bool prefill_path_enabled(const pa_cache_desc& c, int32_t num_q_heads, int32_t num_kv_heads) {
+  const int G = num_q_heads / num_kv_heads;
+  return c.cache_dtype == PA_BF16 && c.head_dim == 128 && G >= 1 && G <= kRowsPerTile &&
+         128 % G == 0;
+}
+
 cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const CUtensorMap& kmap,
-                             const CUtensorMap& vmap, cudaEvent_t before, cudaEvent_t after) {
+                             const CUtensorMap& vmap, const CUtensorMap* qmap,
+                             cudaEvent_t before, cudaEvent_t after) {
   uint8_t* wsb = static_cast<uint8_t*>(a.workspace);
   DecodeParams p{};
   p.q = static_cast<const __nv_bfloat16*>(a.q);
@@ -644,6 +676,7 @@ cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const CUtens
   p.context_lens = a.context_lens;
   p.qsl = a.query_start_loc;
   p.item_start = reinterpret_cast<int32_t*>(wsb + ws.item_start);
+  p.pf_item_start = reinterpret_cast<int32_t*>(wsb + ws.pf_item_start);
   p.part_lse = reinterpret_cast<float*>(wsb + ws.part_lse);
   p.part_o = reinterpret_cast<float*>(wsb + ws.part_o);
   p.out = a.out;
@@ -658,7 +691,9 @@ cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const CUtens
   p.max_query_len = a.max_query_len;
   p.pblk = ws.pblk;
   p.pmax = ws.pmax;
-  p.decode_max_query = ws.decode_max_query;
+  const bool prefill = qmap != nullptr && prefill_path_enabled(a.cache, a.num_q_heads,
+                                                               a.num_kv_heads);
+  p.decode_max_query = prefill ? kDecodeMaxQuery : INT32_MAX;
   p.out_bf16 = a.out_dtype == PA_BF16;
   const float log2e = 1.4426950408889634f;
   const bool fp8 = a.cache.cache_dtype == PA_FP8_E4M3;
@@ -668,6 +703,10 @@ cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const CUtens
   plan_kernel<<<1, 1024, 0, a.stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (prefill) {
+    e = launch_prefill(a, p.pf_item_start, p.hdr, *qmap, kmap, vmap);
+    if (e != cudaSuccess) return e;
+  }
   if (fp8) return run_decode<128, true, 4>(a, ws, p, kmap, vmap, before, after);
   if (a.head_dim == 128) return run_decode<128, false, 3>(a, ws, p, kmap, vmap, before, after);
   return run_decode<64, false, 4>(a, ws, p, kmap, vmap, before, after);

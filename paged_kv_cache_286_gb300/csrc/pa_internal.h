@@ -38,12 +38,12 @@ struct AttnArgs {
 // Workspace carve-up; a pure function of the step's shape (see workspace_layout).
 struct WsLayout {
   size_t item_start;  // int32 [num_seqs + 1], decode work-item prefix sums
+  size_t pf_item_start;  // int32 [num_seqs + 1], prefill work-item prefix sums
   size_t part_lse;    // float [num_q_tokens][num_q_heads][pmax], log2-domain log-sum-exp
   size_t part_o;      // float [num_q_tokens][num_q_heads][pmax][head_dim], normalised partials
   size_t total;
   int32_t pblk;       // blocks per KV partition
   int32_t pmax;       // partitions per sequence at most
-  int32_t decode_max_query;  // sequences with more queries go to the prefill path
 };
 
 WsLayout workspace_layout(int32_t num_seqs, int32_t num_q_tokens, int32_t num_q_heads,
@@ -56,7 +56,20 @@ cudaError_t launch_cache_append(const void* k, const void* v, const int64_t* slo
 
 void set_last_error(const char* msg);
 
+// True when chunks with more than kDecodeMaxQuery queries run on the tcgen05 tile kernel
+// (bf16 pool, head_dim 128, GQA group dividing 128); otherwise every sequence takes the
+// split-KV kernel.
+bool prefill_path_enabled(const pa_cache_desc& c, int32_t num_q_heads, int32_t num_kv_heads);
+
+// `qmap` (3-D view of q) is needed only when the prefill path is enabled and
+// max_query_len > kDecodeMaxQuery; it may be NULL otherwise.
 cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const CUtensorMap& kmap,
-                             const CUtensorMap& vmap, cudaEvent_t before, cudaEvent_t after);
+                             const CUtensorMap& vmap, const CUtensorMap* qmap,
+                             cudaEvent_t before, cudaEvent_t after);
+
+struct WsHeader;
+cudaError_t launch_prefill(const AttnArgs& a, const int32_t* item_start, WsHeader* hdr,
+                           const CUtensorMap& qmap, const CUtensorMap& kmap,
+                           const CUtensorMap& vmap);
 
 }  // namespace pa

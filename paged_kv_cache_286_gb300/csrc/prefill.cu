@@ -1,0 +1,459 @@
+// Causal chunked-prefill tiles on tcgen05 tensor cores.
+//
+// What it computes ("Serving LLMs with vLLM: Continuous Batching and PagedAttention Explained",
+// sections "Chunked Prefill", "Prefill Versus Decode", "Attention Over Scattered Blocks"): a
+// prompt chunk of n tokens whose sequence holds L keys after this step's append sits at
+// positions p_i = L - n + i; token i attends keys 0..p_i, fetched through the block table.
+//
+// Design (GB300 / sm_103a; bf16 K/V, head_dim 128):
+//  * One work item = (sequence, kv head, tile of 128 rows), a row being (query token, q head of
+//    the GQA group), so the tile's queries share every K/V tile they read.  Items are taken
+//    longest-first from an atomic counter by persistent CTAs (one per SM).
+//  * Warp 0 issues TMA copies: the q tile once (a 3-D box of tokens x heads x 64 columns, two
+//    boxes), then for every 128 keys the 8 (block, kv head) K tiles and V tiles of the block
+//    table, into two-stage K and V rings (128-byte swizzle, completion on mbarriers).
+//  * Warp 1 issues tcgen05.mma from one thread: S = Q K^T into one of two TMEM buffers
+//    (128 x 128 fp32), and O += P V into a third (V read MN-major).  P is written by the softmax
+//    threads as bf16 hi + lo parts, so P V is exact to ~2^-16 like the decode path.
+//  * Warps 2-5 own one row each: they read S from TMEM, mask keys beyond the row's position,
+//    keep the running max in the log2 domain and rescale O in TMEM only when the max grows by
+//    more than 2^8 (the final division uses the same max, so the result is exact), write P to
+//    shared memory, and finally divide O by the row sum and store it.
+//  * V rows past the last valid key (stale slots, possibly NaN) are zeroed in shared memory
+//    before P V reads them; K there only feeds masked scores.
+#include <math_constants.h>
+
+#include <algorithm>
+
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace pf {
+constexpr int kRows = 128;
+constexpr int kKeys = 128;
+constexpr int kHalf = 16384;  // one 64-column region of a 128-row bf16 tile
+constexpr int kTile = 32768;  // 128 x 128 bf16
+constexpr int kQ = 0, kPhi = kTile, kPlo = 2 * kTile, kK = 3 * kTile, kV = 5 * kTile;
+constexpr int kCtl = 7 * kTile;  // control block (barriers, item, flags)
+constexpr int kSmem = 1024 + kCtl + 256;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kOCol = 256;
+constexpr float kRescaleLog2 = 8.f;
+}  // namespace pf
+
+struct PrefillParams {
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const int32_t* qsl;
+  const int32_t* item_start;  // [S+1] prefix sums of prefill items
+  void* out;
+  WsHeader* hdr;
+  int32_t max_blocks_per_seq;
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t group;
+  int32_t num_blocks;
+  int32_t out_bf16;
+  float score_log2;
+};
+
+struct PfItem {
+  int s, h, t0, ntok, pos0, L, nkv, nblk_tile, valid;
+};
+
+struct PfCtl {
+  uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full, o_done;
+  uint32_t tmem_base;
+  int abort_flag;
+  int v_zero_from[2];
+  uint32_t v_bad[2];
+  PfItem item;
+};
+static_assert(sizeof(PfCtl) <= 256, "control block too large");
+
+__global__ void __launch_bounds__(pf::kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap qmap,
+                   const __grid_constant__ CUtensorMap kmap,
+                   const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  PfCtl* ctl = reinterpret_cast<PfCtl*>(smem + pf::kCtl);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    mbar_init(&ctl->q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctl->k_full[i], 1);
+      mbar_init(&ctl->k_empty[i], 1);
+      mbar_init(&ctl->v_full[i], 1);
+      mbar_init(&ctl->v_empty[i], 1);
+      mbar_init(&ctl->s_full[i], 1);
+    }
+    mbar_init(&ctl->p_full, pf::kRows);
+    mbar_init(&ctl->o_done, 1);
+    ctl->abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&qmap);
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&vmap);
+  }
+  if (warp == 1) tmem_alloc(&ctl->tmem_base, pf::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  const int total = p.item_start[p.num_seqs];
+  uint32_t tc = 0;  // KV tiles processed by this CTA so far (ring / phase tracking)
+  uint32_t ic = 0;  // items processed by this CTA so far
+  const int G = p.group;
+  const int tpt = pf::kRows / G;  // query tokens per tile
+
+  auto fail = [&](uint32_t bits) {
+    set_error(&p.hdr->error, bits);
+    ctl->abort_flag = 1;
+  };
+  // all lanes wait; the outcome is warp-uniform
+  auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, parity));
+    if (!ok && lane == 0) fail(PA_DEVERR_TIMEOUT);
+    return ok;
+  };
+
+  while (true) {
+    if (tid == 0) {
+      PfItem it;
+      const int rev = static_cast<int>(atomicAdd(&p.hdr->prefill_counter, 1u));
+      const int item = total - 1 - rev;  // longest items (last tiles of a chunk) first
+      it.valid = item >= 0;
+      if (it.valid) {
+        int lo = 0, hi = p.num_seqs;
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (p.item_start[mid] <= item) lo = mid; else hi = mid;
+        }
+        const int s = lo;
+        const int t0 = p.qsl[s];
+        const int n = p.qsl[s + 1] - t0;
+        const int L = p.context_lens[s];
+        const int qtiles = (n + tpt - 1) / tpt;
+        const int local = item - p.item_start[s];
+        const int h = local / qtiles;
+        const int qt = local - h * qtiles;
+        const int i0 = qt * tpt;
+        it.s = s;
+        it.h = h;
+        it.t0 = t0 + i0;
+        it.ntok = min(tpt, n - i0);
+        it.pos0 = L - n + i0;
+        it.L = L;
+        const int pmax = it.pos0 + it.ntok - 1;
+        it.nkv = pmax / pf::kKeys + 1;
+        it.nblk_tile = pmax / kBlockSize + 1;
+      }
+      ctl->item = it;
+    }
+    __syncthreads();
+    const PfItem I = ctl->item;
+    if (!I.valid || ctl->abort_flag) break;
+
+    if (warp == 0) {
+      // ------------------------------------------------------------- producer (TMA) -----
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&ctl->q_full, pf::kTile);
+        tma_load_3d(smem + pf::kQ, &qmap, 0, I.h * G, I.t0, &ctl->q_full);
+        tma_load_3d(smem + pf::kQ + pf::kHalf, &qmap, 64, I.h * G, I.t0, &ctl->q_full);
+      }
+      for (int j = 0; j < I.nkv; ++j) {
+        const uint32_t g = tc + j, st = g & 1u, ph = ((g >> 1) & 1u) ^ 1u;
+        const int jb = 8 * j + lane;
+        int phys = -1;
+        bool bad = false;
+        if (lane < 8 && jb < I.nblk_tile) {
+          phys = __ldg(p.block_tables + static_cast<int64_t>(I.s) * p.max_blocks_per_seq + jb);
+          if (phys < 0 || phys >= p.num_blocks) {
+            set_error(&p.hdr->error, PA_DEVERR_BLOCK_ID);
+            phys = -1;
+            bad = true;
+          }
+        }
+        const uint32_t ok_mask = __ballot_sync(0xffffffffu, phys >= 0);
+        const uint32_t bad_mask = __ballot_sync(0xffffffffu, bad);
+        const uint32_t bytes = __popc(ok_mask) * 2u * 2048u;
+        const int yrow = (phys * p.num_kv_heads + I.h) * kBlockSize;
+        // K tiles of this 128-key slice
+        if (!wait(&ctl->k_empty[st], ph)) break;
+        if (lane == 0) {
+          if (bytes) mbar_arrive_expect_tx(&ctl->k_full[st], bytes);
+          else mbar_arrive(&ctl->k_full[st]);
+        }
+        __syncwarp();
+        if (phys >= 0) {
+          uint8_t* kt = smem + pf::kK + st * pf::kTile + lane * 2048;
+          tma_load_2d(kt, &kmap, 0, yrow, &ctl->k_full[st]);
+          tma_load_2d(kt + pf::kHalf, &kmap, 64, yrow, &ctl->k_full[st]);
+        }
+        // V tiles, with the rows the MMA warp has to clear
+        if (!wait(&ctl->v_empty[st], ph)) break;
+        if (lane == 0) {
+          const int valid_end = min(I.L, I.nblk_tile * kBlockSize) - j * pf::kKeys;
+          ctl->v_zero_from[st] = max(0, min(pf::kKeys, valid_end));
+          ctl->v_bad[st] = bad_mask;
+          if (bytes) mbar_arrive_expect_tx(&ctl->v_full[st], bytes);
+          else mbar_arrive(&ctl->v_full[st]);
+        }
+        __syncwarp();
+        if (phys >= 0) {
+          uint8_t* vt = smem + pf::kV + st * pf::kTile + lane * 2048;
+          tma_load_2d(vt, &vmap, 0, yrow, &ctl->v_full[st]);
+          tma_load_2d(vt + pf::kHalf, &vmap, 64, yrow, &ctl->v_full[st]);
+        }
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------------------- MMA issuer ---------
+      const uint32_t id_s = idesc_bf16_f32(128, 128, false);
+      const uint32_t id_pv = idesc_bf16_f32(128, 128, true);
+      const uint32_t q_addr = smem_u32(smem + pf::kQ);
+      auto issue_s = [&](int j) -> bool {
+        const uint32_t g = tc + j, st = g & 1u;
+        if (!wait(&ctl->k_full[st], (g >> 1) & 1u)) return false;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t k_addr = smem_u32(smem + pf::kK + st * pf::kTile);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t off = (ks >> 2) * pf::kHalf + (ks & 3) * 32;
+            tc_mma_bf16(tmem + st * 128u, smem_desc_sw128(q_addr + off, 16, 1024),
+                        smem_desc_sw128(k_addr + off, 16, 1024), id_s, ks > 0);
+          }
+          tc_commit(&ctl->s_full[st]);
+          tc_commit(&ctl->k_empty[st]);
+        }
+        __syncwarp();
+        return true;
+      };
+      bool ok = wait(&ctl->q_full, ic & 1u);
+      if (ok) tc_fence_after();
+      if (ok) ok = issue_s(0);
+      if (ok && I.nkv > 1) ok = issue_s(1);
+      for (int j = 0; ok && j < I.nkv; ++j) {
+        const uint32_t g = tc + j, st = g & 1u;
+        if (!(ok = wait(&ctl->v_full[st], (g >> 1) & 1u))) break;
+        uint8_t* vt = smem + pf::kV + st * pf::kTile;
+        const int zf = ctl->v_zero_from[st];
+        const uint32_t badm = ctl->v_bad[st];
+        if (zf < pf::kKeys || badm) {
+          // clear the 128-byte rows (both column halves) of keys that hold no valid value
+          for (int e = lane; e < pf::kKeys * 2 * 8; e += 32) {
+            const int key = e >> 4, half = (e >> 3) & 1, c16 = e & 7;
+            if (key >= zf || ((badm >> (key >> 4)) & 1u))
+              *reinterpret_cast<uint4*>(vt + half * pf::kHalf + key * 128 + c16 * 16) =
+                  make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        if (!(ok = wait(&ctl->p_full, g & 1u))) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t v_addr = smem_u32(vt);
+          const uint32_t phi = smem_u32(smem + pf::kPhi), plo = smem_u32(smem + pf::kPlo);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t poff = (ks >> 2) * pf::kHalf + (ks & 3) * 32;
+            tc_mma_bf16(tmem + pf::kOCol, smem_desc_sw128(phi + poff, 16, 1024),
+                        smem_desc_sw128(v_addr + ks * 2048, pf::kHalf, 1024), id_pv,
+                        j > 0 || ks > 0);
+          }
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t poff = (ks >> 2) * pf::kHalf + (ks & 3) * 32;
+            tc_mma_bf16(tmem + pf::kOCol, smem_desc_sw128(plo + poff, 16, 1024),
+                        smem_desc_sw128(v_addr + ks * 2048, pf::kHalf, 1024), id_pv, true);
+          }
+          tc_commit(&ctl->o_done);
+          tc_commit(&ctl->v_empty[st]);
+        }
+        __syncwarp();
+        if (j + 2 < I.nkv) ok = issue_s(j + 2);
+      }
+    } else {
+      // ------------------------------------------------------------- softmax rows -------
+      const int quarter = warp & 3;        // TMEM lane quarter this warp may access
+      const int r = quarter * 32 + lane;   // tile row = TMEM lane
+      const int tok = r / G;
+      const bool row_ok = tok < I.ntok;
+      const int row_pos = I.pos0 + tok;
+      const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+      uint8_t* prow_hi = smem + pf::kPhi + r * 128;
+      uint8_t* prow_lo = smem + pf::kPlo + r * 128;
+      float m_used = 0.f, l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < I.nkv; ++j) {
+        const uint32_t g = tc + j, b = g & 1u;
+        if (!(ok = wait(&ctl->s_full[b], (g >> 1) & 1u))) break;
+        tc_fence_after();
+        const int kmax = row_ok ? row_pos - j * pf::kKeys : -1;  // keys 0..kmax are visible
+        // pass 1: row max of the visible scores
+        float mt = -CUDART_INF_F;
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tl + b * 128u + c * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (c * 32 + i <= kmax) mt = fmaxf(mt, __uint_as_float(v[i]));
+        }
+        mt = (mt == -CUDART_INF_F) ? -CUDART_INF_F : mt * p.score_log2;
+        bool rescale = false;
+        float m_new = m_used;
+        if (j == 0) {
+          m_new = (mt == -CUDART_INF_F) ? 0.f : mt;
+        } else if (mt > m_used + pf::kRescaleLog2) {
+          m_new = mt;
+          rescale = true;
+        }
+        const float alpha = rescale ? fast_exp2(m_used - m_new) : 1.f;
+        const bool warp_rescale = __any_sync(0xffffffffu, rescale);
+        // P (hi/lo) must not be overwritten while the previous P.V still reads it
+        if (j > 0) {
+          if (!(ok = wait(&ctl->o_done, (g - 1) & 1u))) break;
+          tc_fence_after();
+        }
+        // pass 2: probabilities, row sum, bf16 hi/lo P in the swizzled K-major layout
+        float rs = 0.f;
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tl + b * 128u + c * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8) {
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int c0 = c * 32 + q8 * 8 + 2 * e;
+              const float p0 =
+                  (c0 <= kmax)
+                      ? fast_exp2(__fmaf_rn(__uint_as_float(v[q8 * 8 + 2 * e]), p.score_log2, -m_new))
+                      : 0.f;
+              const float p1 = (c0 + 1 <= kmax)
+                                   ? fast_exp2(__fmaf_rn(__uint_as_float(v[q8 * 8 + 2 * e + 1]),
+                                                         p.score_log2, -m_new))
+                                   : 0.f;
+              rs += p0 + p1;
+              hi[e] = pack_bf16x2(p0, p1);
+              lo[e] = pack_bf16x2(p0 - bf16lo_to_f32(hi[e]), p1 - bf16hi_to_f32(hi[e]));
+            }
+            const int chunk = c * 4 + q8;  // 16-byte chunk = 8 keys
+            const int off = (chunk >> 3) * pf::kHalf + ((((chunk & 7) ^ (r & 7))) << 4);
+            *reinterpret_cast<uint4*>(prow_hi + off) =
+                make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(prow_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          }
+        }
+        l = l * alpha + rs;
+        if (warp_rescale) {
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tl + pf::kOCol + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tl + pf::kOCol + c * 32, o);
+          }
+          tmem_wait_st();
+        }
+        m_used = m_new;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&ctl->p_full);
+      }
+      // epilogue: O / l
+      if (ok && wait(&ctl->o_done, (tc + I.nkv - 1) & 1u)) {
+        tc_fence_after();
+        const float inv = (row_ok && l > 0.f) ? 1.f / l : 0.f;
+        const int64_t orow = static_cast<int64_t>(I.t0 + tok) * p.num_q_heads + I.h * G + r % G;
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tl + pf::kOCol + c * 32, o);
+          tmem_wait_ld();
+          if (row_ok) {
+            if (p.out_bf16) {
+              uint4* dst = reinterpret_cast<uint4*>(
+                  reinterpret_cast<__nv_bfloat16*>(p.out) + orow * 128 + c * 32);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  w[e] = pack_bf16x2(__uint_as_float(o[8 * i + 2 * e]) * inv,
+                                     __uint_as_float(o[8 * i + 2 * e + 1]) * inv);
+                dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+              }
+            } else {
+              float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) +
+                                                      orow * 128 + c * 32);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv,
+                                     __uint_as_float(o[4 * i + 1]) * inv,
+                                     __uint_as_float(o[4 * i + 2]) * inv,
+                                     __uint_as_float(o[4 * i + 3]) * inv);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+    }
+    tc += I.nkv;
+    ++ic;
+    __syncthreads();
+    tc_fence_after();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, pf::kTmemCols);
+}
+
+size_t prefill_smem_bytes() { return pf::kSmem; }
+
+cudaError_t launch_prefill(const AttnArgs& a, const int32_t* item_start, WsHeader* hdr,
+                           const CUtensorMap& qmap, const CUtensorMap& kmap,
+                           const CUtensorMap& vmap) {
+  PrefillParams p{};
+  p.block_tables = a.block_tables;
+  p.context_lens = a.context_lens;
+  p.qsl = a.query_start_loc;
+  p.item_start = item_start;
+  p.out = a.out;
+  p.hdr = hdr;
+  p.max_blocks_per_seq = a.max_blocks_per_seq;
+  p.num_seqs = a.num_seqs;
+  p.num_q_heads = a.num_q_heads;
+  p.num_kv_heads = a.num_kv_heads;
+  p.group = a.num_q_heads / a.num_kv_heads;
+  p.num_blocks = a.cache.num_blocks;
+  p.out_bf16 = a.out_dtype == PA_BF16;
+  p.score_log2 = a.scale * 1.4426950408889634f;
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       pf::kSmem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int G = p.group;
+  const int64_t upper =
+      static_cast<int64_t>(a.num_kv_heads) *
+      ((static_cast<int64_t>(a.num_q_tokens) * G + pf::kRows - 1) / pf::kRows + a.num_seqs);
+  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(upper, sms));
+  prefill_kernel<<<static_cast<unsigned>(grid), pf::kThreads, pf::kSmem, a.stream>>>(qmap, kmap,
+                                                                                     vmap, p);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -84,6 +84,41 @@ def test_multi_query_causal(qlens, ctx, dtype):
     _check_small(w)
 
 
+PF_CTX = [700, 17, 300, 1000, 129, 2100]
+PF_QL = [200, 17, 300, 33, 129, 64]
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 8), (32, 8), (64, 8)])
+def test_prefill_chunks_on_tensor_core_tiles(hq, hkv):
+    """Chunks with more than 16 queries take the tcgen05 tile path (bf16, head_dim 128):
+    several 128-row tiles and 128-key slices, chunks with and without a cached prefix, ragged
+    last blocks holding NaN patterns, GQA groups 1, 2, 4, 8, mixed with decode sequences."""
+    w = make_workload(PF_CTX + [90, 3000], PF_QL + [1, 1], num_q_heads=hq, num_kv_heads=hkv,
+                      head_dim=128, seed=hq * 7 + 1, pool_fill="nan")
+    _check_small(w)
+
+
+def test_prefill_chunks_bf16_output():
+    w = make_workload(PF_CTX, PF_QL, num_q_heads=32, num_kv_heads=8, head_dim=128, seed=91)
+    _check_small(w, out_dtype=torch.bfloat16)
+
+
+def test_prefill_block_permutation_is_bitwise_invariant():
+    h = _h()
+    args = dict(num_q_heads=32, num_kv_heads=8, head_dim=128, seed=92, pool_factor=1.5)
+    w = make_workload([600, 300], [400, 300], **args)
+    _, out1 = h.run_gpu(w)
+    out1 = out1.clone()
+    perm = np.random.default_rng(2).permutation(w.num_blocks)
+    w2 = make_workload([600, 300], [400, 300], **args)
+    w2.block_tables = np.where(w.block_tables >= 0, perm[np.maximum(w.block_tables, 0)], -1) \
+        .astype(np.int32)
+    w2.slot_mapping = perm[w.slot_mapping // 16] * 16 + w.slot_mapping % 16
+    w2.slot_prior = perm[w.slot_prior // 16] * 16 + w.slot_prior % 16
+    _, out2 = h.run_gpu(w2)
+    assert torch.equal(out1, out2)
+
+
 def test_single_sequence_long_context_splits():
     w = make_workload([9000], [1], num_q_heads=8, num_kv_heads=2, head_dim=128, seed=5)
     _check_small(w)
