@@ -11,14 +11,16 @@
 //    longest-first from an atomic counter by persistent CTAs (one per SM).
 //  * Warp 0 issues TMA copies: the q tile once (a 3-D box of tokens x heads x 64 columns, two
 //    boxes), then for every 128 keys the 8 (block, kv head) K tiles and V tiles of the block
-//    table, into two-stage K and V rings (128-byte swizzle, completion on mbarriers).
+//    table, into three-stage K and V rings (128-byte swizzle, completion on mbarriers).
 //  * Warp 1 issues tcgen05.mma from one thread: S = Q K^T into one of two TMEM buffers
-//    (128 x 128 fp32), and O += P V into a third (V read MN-major).  P is written by the softmax
-//    threads as bf16 hi + lo parts, so P V is exact to ~2^-16 like the decode path.
-//  * Warps 2-5 own one row each: they read S from TMEM, mask keys beyond the row's position,
-//    keep the running max in the log2 domain and rescale O in TMEM only when the max grows by
-//    more than 2^8 (the final division uses the same max, so the result is exact), write P to
-//    shared memory, and finally divide O by the row sum and store it.
+//    (128 x 128 fp32), and O += P V into a third, with P read from TMEM and V from shared
+//    memory (MN-major).  The softmax threads write P back over their S buffer as bf16 hi and lo
+//    halves (64 columns each), so P V is exact to ~2^-16 like the decode path, and the next
+//    tile's softmax can run while this tile's P V is in flight.
+//  * Warps 2-5 own one row each: they read the row of S from TMEM once, mask keys beyond the
+//    row's position, keep the running max in the log2 domain and rescale O in TMEM only when
+//    the max grows by more than 2^8 (the final division uses the same max, so the result is
+//    exact), and finally divide O by the row sum and store it.
 //  * V rows past the last valid key (stale slots, possibly NaN) are zeroed in shared memory
 //    before P V reads them; K there only feeds masked scores.
 #include <math_constants.h>
@@ -33,10 +35,11 @@ namespace pa {
 namespace pf {
 constexpr int kRows = 128;
 constexpr int kKeys = 128;
+constexpr int kStages = 3;
 constexpr int kHalf = 16384;  // one 64-column region of a 128-row bf16 tile
 constexpr int kTile = 32768;  // 128 x 128 bf16
-constexpr int kQ = 0, kPhi = kTile, kPlo = 2 * kTile, kK = 3 * kTile, kV = 5 * kTile;
-constexpr int kCtl = 7 * kTile;  // control block (barriers, item, flags)
+constexpr int kQ = 0, kK = kTile, kV = kK + kStages * kTile;
+constexpr int kCtl = kV + kStages * kTile;  // control block (barriers, item, flags)
 constexpr int kSmem = 1024 + kCtl + 256;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
@@ -66,11 +69,12 @@ struct PfItem {
 };
 
 struct PfCtl {
-  uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full, o_done;
+  uint64_t q_full, k_full[pf::kStages], k_empty[pf::kStages], v_full[pf::kStages],
+      v_empty[pf::kStages], s_full[2], p_full[2], o_done[2];
   uint32_t tmem_base;
   int abort_flag;
-  int v_zero_from[2];
-  uint32_t v_bad[2];
+  int v_zero_from[pf::kStages];
+  uint32_t v_bad[pf::kStages];
   PfItem item;
 };
 static_assert(sizeof(PfCtl) <= 256, "control block too large");
@@ -87,15 +91,19 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
 
   if (tid == 0) {
     mbar_init(&ctl->q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < pf::kStages; ++i) {
       mbar_init(&ctl->k_full[i], 1);
       mbar_init(&ctl->k_empty[i], 1);
       mbar_init(&ctl->v_full[i], 1);
       mbar_init(&ctl->v_empty[i], 1);
-      mbar_init(&ctl->s_full[i], 1);
     }
-    mbar_init(&ctl->p_full, pf::kRows);
-    mbar_init(&ctl->o_done, 1);
+    // one of each per S/P buffer, so that every waiter is within one phase of its barrier:
+    // S of tile g+2 is issued only after P V of tile g, which waits for P of tile g
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctl->s_full[i], 1);
+      mbar_init(&ctl->p_full[i], pf::kRows);
+      mbar_init(&ctl->o_done[i], 1);
+    }
     ctl->abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&qmap);
@@ -169,7 +177,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         tma_load_3d(smem + pf::kQ + pf::kHalf, &qmap, 64, I.h * G, I.t0, &ctl->q_full);
       }
       for (int j = 0; j < I.nkv; ++j) {
-        const uint32_t g = tc + j, st = g & 1u, ph = ((g >> 1) & 1u) ^ 1u;
+        const uint32_t g = tc + j, st = g % pf::kStages;
+        const uint32_t ph = ((g / pf::kStages) & 1u) ^ 1u;
         const int jb = 8 * j + lane;
         int phys = -1;
         bool bad = false;
@@ -219,18 +228,18 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       const uint32_t id_pv = idesc_bf16_f32(128, 128, true);
       const uint32_t q_addr = smem_u32(smem + pf::kQ);
       auto issue_s = [&](int j) -> bool {
-        const uint32_t g = tc + j, st = g & 1u;
-        if (!wait(&ctl->k_full[st], (g >> 1) & 1u)) return false;
+        const uint32_t g = tc + j, st = g % pf::kStages, b = g & 1u;
+        if (!wait(&ctl->k_full[st], (g / pf::kStages) & 1u)) return false;
         tc_fence_after();
         if (lane == 0) {
           const uint32_t k_addr = smem_u32(smem + pf::kK + st * pf::kTile);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t off = (ks >> 2) * pf::kHalf + (ks & 3) * 32;
-            tc_mma_bf16(tmem + st * 128u, smem_desc_sw128(q_addr + off, 16, 1024),
+            tc_mma_bf16(tmem + b * 128u, smem_desc_sw128(q_addr + off, 16, 1024),
                         smem_desc_sw128(k_addr + off, 16, 1024), id_s, ks > 0);
           }
-          tc_commit(&ctl->s_full[st]);
+          tc_commit(&ctl->s_full[b]);
           tc_commit(&ctl->k_empty[st]);
         }
         __syncwarp();
@@ -241,8 +250,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       if (ok) ok = issue_s(0);
       if (ok && I.nkv > 1) ok = issue_s(1);
       for (int j = 0; ok && j < I.nkv; ++j) {
-        const uint32_t g = tc + j, st = g & 1u;
-        if (!(ok = wait(&ctl->v_full[st], (g >> 1) & 1u))) break;
+        const uint32_t g = tc + j, st = g % pf::kStages, b = g & 1u;
+        if (!(ok = wait(&ctl->v_full[st], (g / pf::kStages) & 1u))) break;
         uint8_t* vt = smem + pf::kV + st * pf::kTile;
         const int zf = ctl->v_zero_from[st];
         const uint32_t badm = ctl->v_bad[st];
@@ -257,28 +266,26 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
         }
-        if (!(ok = wait(&ctl->p_full, g & 1u))) break;
+        if (!(ok = wait(&ctl->p_full[b], (g >> 1) & 1u))) break;
         tc_fence_after();
         if (lane == 0) {
           const uint32_t v_addr = smem_u32(vt);
-          const uint32_t phi = smem_u32(smem + pf::kPhi), plo = smem_u32(smem + pf::kPlo);
+          const uint32_t p_hi = tmem + b * 128u, p_lo = p_hi + 64u;
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t poff = (ks >> 2) * pf::kHalf + (ks & 3) * 32;
-            tc_mma_bf16(tmem + pf::kOCol, smem_desc_sw128(phi + poff, 16, 1024),
-                        smem_desc_sw128(v_addr + ks * 2048, pf::kHalf, 1024), id_pv,
-                        j > 0 || ks > 0);
-          }
+          for (int ks = 0; ks < 8; ++ks)
+            tc_mma_bf16_ts(tmem + pf::kOCol, p_hi + ks * 8,
+                           smem_desc_sw128(v_addr + ks * 2048, pf::kHalf, 1024), id_pv,
+                           j > 0 || ks > 0);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t poff = (ks >> 2) * pf::kHalf + (ks & 3) * 32;
-            tc_mma_bf16(tmem + pf::kOCol, smem_desc_sw128(plo + poff, 16, 1024),
-                        smem_desc_sw128(v_addr + ks * 2048, pf::kHalf, 1024), id_pv, true);
-          }
-          tc_commit(&ctl->o_done);
+          for (int ks = 0; ks < 8; ++ks)
+            tc_mma_bf16_ts(tmem + pf::kOCol, p_lo + ks * 8,
+                           smem_desc_sw128(v_addr + ks * 2048, pf::kHalf, 1024), id_pv, true);
+          tc_commit(&ctl->o_done[b]);
           tc_commit(&ctl->v_empty[st]);
         }
         __syncwarp();
+        // S of tile j+2 reuses this tile's S/P buffer: it is issued after (and runs after) the
+        // P V that reads P from it
         if (j + 2 < I.nkv) ok = issue_s(j + 2);
       }
     } else {
@@ -289,8 +296,6 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       const bool row_ok = tok < I.ntok;
       const int row_pos = I.pos0 + tok;
       const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-      uint8_t* prow_hi = smem + pf::kPhi + r * 128;
-      uint8_t* prow_lo = smem + pf::kPlo + r * 128;
       float m_used = 0.f, l = 0.f;
       bool ok = true;
       for (int j = 0; j < I.nkv; ++j) {
@@ -298,17 +303,26 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         if (!(ok = wait(&ctl->s_full[b], (g >> 1) & 1u))) break;
         tc_fence_after();
         const int kmax = row_ok ? row_pos - j * pf::kKeys : -1;  // keys 0..kmax are visible
-        // pass 1: row max of the visible scores
-        float mt = -CUDART_INF_F;
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tl + b * 128u + c * 32, v);
-          tmem_wait_ld();
+        uint32_t sv[128];
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (c * 32 + i <= kmax) mt = fmaxf(mt, __uint_as_float(v[i]));
+        for (int c = 0; c < 4; ++c)
+          tmem_ld32(tl + b * 128u + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
+        tmem_wait_ld();
+        float x[128];
+        float mt = -CUDART_INF_F;
+        if (kmax >= pf::kKeys - 1) {
+#pragma unroll
+          for (int i = 0; i < 128; ++i) {
+            x[i] = __uint_as_float(sv[i]) * p.score_log2;
+            mt = fmaxf(mt, x[i]);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 128; ++i) {
+            x[i] = (i <= kmax) ? __uint_as_float(sv[i]) * p.score_log2 : -CUDART_INF_F;
+            mt = fmaxf(mt, x[i]);
+          }
         }
-        mt = (mt == -CUDART_INF_F) ? -CUDART_INF_F : mt * p.score_log2;
         bool rescale = false;
         float m_new = m_used;
         if (j == 0) {
@@ -318,92 +332,75 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           rescale = true;
         }
         const float alpha = rescale ? fast_exp2(m_used - m_new) : 1.f;
-        const bool warp_rescale = __any_sync(0xffffffffu, rescale);
-        // P (hi/lo) must not be overwritten while the previous P.V still reads it
-        if (j > 0) {
-          if (!(ok = wait(&ctl->o_done, (g - 1) & 1u))) break;
-          tc_fence_after();
-        }
-        // pass 2: probabilities, row sum, bf16 hi/lo P in the swizzled K-major layout
+        // probabilities; bf16 hi halves into columns 0..63 of the buffer, lo into 64..127
         float rs = 0.f;
+#pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tl + b * 128u + c * 32, v);
-          tmem_wait_ld();
+          uint32_t hi[16], lo[16];
 #pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {
-            uint32_t hi[4], lo[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c0 = c * 32 + q8 * 8 + 2 * e;
-              const float p0 =
-                  (c0 <= kmax)
-                      ? fast_exp2(__fmaf_rn(__uint_as_float(v[q8 * 8 + 2 * e]), p.score_log2, -m_new))
-                      : 0.f;
-              const float p1 = (c0 + 1 <= kmax)
-                                   ? fast_exp2(__fmaf_rn(__uint_as_float(v[q8 * 8 + 2 * e + 1]),
-                                                         p.score_log2, -m_new))
-                                   : 0.f;
-              rs += p0 + p1;
-              hi[e] = pack_bf16x2(p0, p1);
-              lo[e] = pack_bf16x2(p0 - bf16lo_to_f32(hi[e]), p1 - bf16hi_to_f32(hi[e]));
-            }
-            const int chunk = c * 4 + q8;  // 16-byte chunk = 8 keys
-            const int off = (chunk >> 3) * pf::kHalf + ((((chunk & 7) ^ (r & 7))) << 4);
-            *reinterpret_cast<uint4*>(prow_hi + off) =
-                make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(prow_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = fast_exp2(x[c * 32 + 2 * e] - m_new);
+            const float p1 = fast_exp2(x[c * 32 + 2 * e + 1] - m_new);
+            rs += p0 + p1;
+            hi[e] = pack_bf16x2(p0, p1);
+            lo[e] = pack_bf16x2(p0 - bf16lo_to_f32(hi[e]), p1 - bf16hi_to_f32(hi[e]));
           }
+          tmem_st16(tl + b * 128u + c * 16, hi);
+          tmem_st16(tl + b * 128u + 64 + c * 16, lo);
         }
         l = l * alpha + rs;
-        if (warp_rescale) {
-          for (int c = 0; c < 4; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tl + pf::kOCol + c * 32, o);
-            tmem_wait_ld();
+        if (__any_sync(0xffffffffu, rescale)) {
+          // O may be rescaled only once the previous P V has landed in it
+          if (j > 0 && !(ok = wait(&ctl->o_done[(g - 1) & 1u], ((g - 1) >> 1) & 1u))) break;
+          tc_fence_after();
+          uint32_t o[128];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tl + pf::kOCol + c * 32, o);
-          }
-          tmem_wait_st();
+          for (int c = 0; c < 4; ++c)
+            tmem_ld32(tl + pf::kOCol + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&o[c * 32]));
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 128; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            tmem_st32(tl + pf::kOCol + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&o[c * 32]));
         }
+        tmem_wait_st();
         m_used = m_new;
-        fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&ctl->p_full);
+        mbar_arrive(&ctl->p_full[b]);
       }
       // epilogue: O / l
-      if (ok && wait(&ctl->o_done, (tc + I.nkv - 1) & 1u)) {
+      const uint32_t g_last = tc + I.nkv - 1;
+      if (ok && wait(&ctl->o_done[g_last & 1u], (g_last >> 1) & 1u)) {
         tc_fence_after();
         const float inv = (row_ok && l > 0.f) ? 1.f / l : 0.f;
         const int64_t orow = static_cast<int64_t>(I.t0 + tok) * p.num_q_heads + I.h * G + r % G;
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tl + pf::kOCol + c * 32, o);
-          tmem_wait_ld();
-          if (row_ok) {
-            if (p.out_bf16) {
-              uint4* dst = reinterpret_cast<uint4*>(
-                  reinterpret_cast<__nv_bfloat16*>(p.out) + orow * 128 + c * 32);
+        uint32_t o[128];
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                uint32_t w[4];
+        for (int c = 0; c < 4; ++c)
+          tmem_ld32(tl + pf::kOCol + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&o[c * 32]));
+        tmem_wait_ld();
+        if (row_ok) {
+          if (p.out_bf16) {
+            uint4* dst =
+                reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * 128);
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                  w[e] = pack_bf16x2(__uint_as_float(o[8 * i + 2 * e]) * inv,
-                                     __uint_as_float(o[8 * i + 2 * e + 1]) * inv);
-                dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
-              }
-            } else {
-              float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) +
-                                                      orow * 128 + c * 32);
+            for (int i = 0; i < 16; ++i) {
+              uint32_t w[4];
 #pragma unroll
-              for (int i = 0; i < 8; ++i)
-                dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv,
-                                     __uint_as_float(o[4 * i + 1]) * inv,
-                                     __uint_as_float(o[4 * i + 2]) * inv,
-                                     __uint_as_float(o[4 * i + 3]) * inv);
+              for (int e = 0; e < 4; ++e)
+                w[e] = pack_bf16x2(__uint_as_float(o[8 * i + 2 * e]) * inv,
+                                   __uint_as_float(o[8 * i + 2 * e + 1]) * inv);
+              dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
             }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + orow * 128);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv,
+                                   __uint_as_float(o[4 * i + 1]) * inv,
+                                   __uint_as_float(o[4 * i + 2]) * inv,
+                                   __uint_as_float(o[4 * i + 3]) * inv);
           }
         }
       }
