@@ -223,15 +223,18 @@ class DeviceWorkload:
         self.out_host.copy_(self.out, non_blocking=True)
 
     def launches_per_step(self) -> int:
-        """Our kernels one step launches: append, plan, attention, and the LSE merge when the
-        workspace carries split partials (it does exactly when a sequence can span more than
-        one KV partition)."""
+        """Our kernels one step launches: the append, the plan, the split-KV attention, the LSE
+        merge when the workspace carries split partials, and the tensor-core prefill kernel
+        when the step holds chunks of more than 16 queries over a bf16 pool with head_dim 128."""
         w = self.w
         size = self.pa.attention_workspace_size(w.num_seqs, w.num_tokens, w.num_q_heads,
                                                 w.num_kv_heads, w.head_dim, w.max_context_len,
                                                 w.max_query_len)
-        no_partials = 256 + ((4 * (w.num_seqs + 1) + 255) // 256) * 256
-        return 3 + (1 if size > no_partials else 0)
+        no_partials = 256 + 2 * (((4 * (w.num_seqs + 1) + 255) // 256) * 256)
+        g = w.num_q_heads // w.num_kv_heads
+        prefill = (w.max_query_len > 16 and w.cache_dtype == "bf16" and w.head_dim == 128
+                   and 128 % g == 0)
+        return 3 + (1 if size > no_partials else 0) + (1 if prefill else 0)
 
 
 def decode_src_sha() -> str:

@@ -175,7 +175,7 @@ struct ItemInfo {
 };
 
 template <int D, bool kFp8, int NST>
-__global__ void __launch_bounds__(kDecodeWarps * 32)
+__global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     decode_kernel(const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
   using C = DecodeCfg<D, kFp8>;
@@ -393,8 +393,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
               for (int m = 0; m < 4; ++m) {
                 const int ks = 4 * kk + m;
                 const uint32_t a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
-                mma_f16(sacc[nt], a, e4m3x2_to_f16x2(static_cast<uint16_t>(r[m] & 0xffffu)),
-                        e4m3x2_to_f16x2(static_cast<uint16_t>(r[m] >> 16)));
+                uint32_t b0, b1;
+                e4m3x4_to_f16x2x2(r[m], b0, b1);
+                mma_f16(sacc[nt], a, b0, b1);
               }
             }
           }
@@ -479,12 +480,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
             r[3] &= vm_hi;
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
-              const uint32_t lo = r[2 * h2], hi = r[2 * h2 + 1];
-              const uint32_t a[4] = {
-                  e4m3x2_to_f16x2(static_cast<uint16_t>(prmt(lo, 0u, 0x0020u))),
-                  e4m3x2_to_f16x2(static_cast<uint16_t>(prmt(lo, 0u, 0x0031u))),
-                  e4m3x2_to_f16x2(static_cast<uint16_t>(prmt(hi, 0u, 0x0020u))),
-                  e4m3x2_to_f16x2(static_cast<uint16_t>(prmt(hi, 0u, 0x0031u)))};
+              // bytes (b0, b2) -> keys 2qc, 2qc+1 at d 2u; (b1, b3) -> the same keys at d 2u+1
+              uint32_t a[4];
+              e4m3x4_to_f16x2x2(prmt(r[2 * h2], 0u, 0x3120u), a[0], a[1]);
+              e4m3x4_to_f16x2x2(prmt(r[2 * h2 + 1], 0u, 0x3120u), a[2], a[3]);
               mma_f16(oacc[2 * jj + h2], a, pf0, pf1);
             }
           }

@@ -175,6 +175,16 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
   return out;
 }
 
+// Four E4M3 bytes of one register to two exact f16x2: bytes 0,1 -> *lo, bytes 2,3 -> *hi.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(four));
+}
+
 // Two fp32 to E4M3 bytes, round to nearest even, saturating: `lo` -> low byte.
 __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
   uint16_t out;

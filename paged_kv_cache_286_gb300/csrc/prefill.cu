@@ -308,21 +308,27 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         for (int c = 0; c < 4; ++c)
           tmem_ld32(tl + b * 128u + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
         tmem_wait_ld();
+        // scores in the log2 domain; masked keys become -inf.  Eight independent max / sum
+        // accumulators keep the dependency chains short.
         float x[128];
-        float mt = -CUDART_INF_F;
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = -CUDART_INF_F;
         if (kmax >= pf::kKeys - 1) {
 #pragma unroll
           for (int i = 0; i < 128; ++i) {
             x[i] = __uint_as_float(sv[i]) * p.score_log2;
-            mt = fmaxf(mt, x[i]);
+            mx[i & 7] = fmaxf(mx[i & 7], x[i]);
           }
         } else {
 #pragma unroll
           for (int i = 0; i < 128; ++i) {
             x[i] = (i <= kmax) ? __uint_as_float(sv[i]) * p.score_log2 : -CUDART_INF_F;
-            mt = fmaxf(mt, x[i]);
+            mx[i & 7] = fmaxf(mx[i & 7], x[i]);
           }
         }
+        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         bool rescale = false;
         float m_new = m_used;
         if (j == 0) {
@@ -333,7 +339,9 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         }
         const float alpha = rescale ? fast_exp2(m_used - m_new) : 1.f;
         // probabilities; bf16 hi halves into columns 0..63 of the buffer, lo into 64..127
-        float rs = 0.f;
+        float rsum[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rsum[i] = 0.f;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t hi[16], lo[16];
@@ -341,13 +349,15 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           for (int e = 0; e < 16; ++e) {
             const float p0 = fast_exp2(x[c * 32 + 2 * e] - m_new);
             const float p1 = fast_exp2(x[c * 32 + 2 * e + 1] - m_new);
-            rs += p0 + p1;
+            rsum[e & 7] += p0 + p1;
             hi[e] = pack_bf16x2(p0, p1);
             lo[e] = pack_bf16x2(p0 - bf16lo_to_f32(hi[e]), p1 - bf16hi_to_f32(hi[e]));
           }
           tmem_st16(tl + b * 128u + c * 16, hi);
           tmem_st16(tl + b * 128u + 64 + c * 16, lo);
         }
+        const float rs = ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3])) +
+                         ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
         l = l * alpha + rs;
         if (__any_sync(0xffffffffu, rescale)) {
           // O may be rescaled only once the previous P V has landed in it
