@@ -35,7 +35,8 @@ namespace pa {
 namespace pf {
 constexpr int kRows = 128;
 constexpr int kKeys = 128;
-constexpr int kStages = 3;
+constexpr int kStages = 3;   // K and V ring depth
+constexpr int kSBufs = 3;    // S/P buffers in TMEM (3 x 128 columns) ahead of O
 constexpr int kHalf = 16384;  // one 64-column region of a 128-row bf16 tile
 constexpr int kTile = 32768;  // 128 x 128 bf16
 constexpr int kQ = 0, kK = kTile, kV = kK + kStages * kTile;
@@ -43,7 +44,7 @@ constexpr int kCtl = kV + kStages * kTile;  // control block (barriers, item, fl
 constexpr int kSmem = 1024 + kCtl + 256;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kOCol = 256;
+constexpr uint32_t kOCol = kSBufs * 128;
 constexpr float kRescaleLog2 = 8.f;
 }  // namespace pf
 
@@ -70,7 +71,7 @@ struct PfItem {
 
 struct PfCtl {
   uint64_t q_full, k_full[pf::kStages], k_empty[pf::kStages], v_full[pf::kStages],
-      v_empty[pf::kStages], s_full[2], p_full[2], o_done[2];
+      v_empty[pf::kStages], s_full[pf::kSBufs], p_full[pf::kSBufs], o_done[pf::kSBufs];
   uint32_t tmem_base;
   int abort_flag;
   int v_zero_from[pf::kStages];
@@ -98,8 +99,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       mbar_init(&ctl->v_empty[i], 1);
     }
     // one of each per S/P buffer, so that every waiter is within one phase of its barrier:
-    // S of tile g+2 is issued only after P V of tile g, which waits for P of tile g
-    for (int i = 0; i < 2; ++i) {
+    // S of tile g+3 is issued only after P V of tile g, which waits for P of tile g
+    for (int i = 0; i < pf::kSBufs; ++i) {
       mbar_init(&ctl->s_full[i], 1);
       mbar_init(&ctl->p_full[i], pf::kRows);
       mbar_init(&ctl->o_done[i], 1);
@@ -176,51 +177,93 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         tma_load_3d(smem + pf::kQ, &qmap, 0, I.h * G, I.t0, &ctl->q_full);
         tma_load_3d(smem + pf::kQ + pf::kHalf, &qmap, 64, I.h * G, I.t0, &ctl->q_full);
       }
-      for (int j = 0; j < I.nkv; ++j) {
-        const uint32_t g = tc + j, st = g % pf::kStages;
-        const uint32_t ph = ((g / pf::kStages) & 1u) ^ 1u;
+      // Block-table entries are read 32 at a time (lane l holds block 32 * grp + l) with the
+      // next group prefetched, so no TMA issue waits on a dependent table load.
+      const int32_t* trow = p.block_tables + static_cast<int64_t>(I.s) * p.max_blocks_per_seq;
+      auto tab_load = [&](int grp) -> int {
+        const int jb = 32 * grp + lane;
+        return jb < I.nblk_tile ? __ldg(trow + jb) : -1;
+      };
+      int grp_cur = 0;
+      int tab_cur = tab_load(0);
+      int tab_next = tab_load(1);
+      // block ids of slice j for lanes 0-7 (-1 = not loaded), plus masks of loadable / bad ones
+      auto slice = [&](int j, int& phys, uint32_t& ok_mask, uint32_t& bad_mask) {
+        const int grp = j >> 2;
+        if (grp != grp_cur) {
+          tab_cur = tab_next;
+          tab_next = tab_load(grp + 1);
+          grp_cur = grp;
+        }
+        const int e = __shfl_sync(0xffffffffu, tab_cur, 8 * (j & 3) + (lane & 7));
         const int jb = 8 * j + lane;
-        int phys = -1;
+        phys = -1;
         bool bad = false;
         if (lane < 8 && jb < I.nblk_tile) {
-          phys = __ldg(p.block_tables + static_cast<int64_t>(I.s) * p.max_blocks_per_seq + jb);
-          if (phys < 0 || phys >= p.num_blocks) {
+          if (e < 0 || e >= p.num_blocks) {
             set_error(&p.hdr->error, PA_DEVERR_BLOCK_ID);
-            phys = -1;
             bad = true;
+          } else {
+            phys = e;
           }
         }
-        const uint32_t ok_mask = __ballot_sync(0xffffffffu, phys >= 0);
-        const uint32_t bad_mask = __ballot_sync(0xffffffffu, bad);
-        const uint32_t bytes = __popc(ok_mask) * 2u * 2048u;
-        const int yrow = (phys * p.num_kv_heads + I.h) * kBlockSize;
-        // K tiles of this 128-key slice
-        if (!wait(&ctl->k_empty[st], ph)) break;
+        ok_mask = __ballot_sync(0xffffffffu, phys >= 0);
+        bad_mask = __ballot_sync(0xffffffffu, bad);
+      };
+      auto load_k = [&](int j, int phys, uint32_t okm) -> bool {
+        const uint32_t g = tc + j, st = g % pf::kStages;
+        const uint32_t bytes = __popc(okm) * 2u * 2048u;
+        if (!wait(&ctl->k_empty[st], ((g / pf::kStages) & 1u) ^ 1u)) return false;
         if (lane == 0) {
           if (bytes) mbar_arrive_expect_tx(&ctl->k_full[st], bytes);
           else mbar_arrive(&ctl->k_full[st]);
         }
         __syncwarp();
         if (phys >= 0) {
+          const int yrow = (phys * p.num_kv_heads + I.h) * kBlockSize;
           uint8_t* kt = smem + pf::kK + st * pf::kTile + lane * 2048;
           tma_load_2d(kt, &kmap, 0, yrow, &ctl->k_full[st]);
           tma_load_2d(kt + pf::kHalf, &kmap, 64, yrow, &ctl->k_full[st]);
         }
-        // V tiles, with the rows the MMA warp has to clear
-        if (!wait(&ctl->v_empty[st], ph)) break;
+        return true;
+      };
+      auto load_v = [&](int j, int phys, uint32_t okm, uint32_t badm) -> bool {
+        const uint32_t g = tc + j, st = g % pf::kStages;
+        const uint32_t bytes = __popc(okm) * 2u * 2048u;
+        if (!wait(&ctl->v_empty[st], ((g / pf::kStages) & 1u) ^ 1u)) return false;
         if (lane == 0) {
+          // rows the MMA warp has to clear: keys past the last valid one, and bad blocks
           const int valid_end = min(I.L, I.nblk_tile * kBlockSize) - j * pf::kKeys;
           ctl->v_zero_from[st] = max(0, min(pf::kKeys, valid_end));
-          ctl->v_bad[st] = bad_mask;
+          ctl->v_bad[st] = badm;
           if (bytes) mbar_arrive_expect_tx(&ctl->v_full[st], bytes);
           else mbar_arrive(&ctl->v_full[st]);
         }
         __syncwarp();
         if (phys >= 0) {
+          const int yrow = (phys * p.num_kv_heads + I.h) * kBlockSize;
           uint8_t* vt = smem + pf::kV + st * pf::kTile + lane * 2048;
           tma_load_2d(vt, &vmap, 0, yrow, &ctl->v_full[st]);
           tma_load_2d(vt + pf::kHalf, &vmap, 64, yrow, &ctl->v_full[st]);
         }
+        return true;
+      };
+      // K runs one slice ahead of V: S needs K three tiles before P V needs V
+      int ph_cur;
+      uint32_t ok_cur, bad_cur;
+      slice(0, ph_cur, ok_cur, bad_cur);
+      bool pok = load_k(0, ph_cur, ok_cur);
+      for (int j = 0; pok && j < I.nkv; ++j) {
+        int ph_nxt = -1;
+        uint32_t ok_nxt = 0, bad_nxt = 0;
+        if (j + 1 < I.nkv) {
+          slice(j + 1, ph_nxt, ok_nxt, bad_nxt);
+          pok = load_k(j + 1, ph_nxt, ok_nxt);
+        }
+        if (pok) pok = load_v(j, ph_cur, ok_cur, bad_cur);
+        ph_cur = ph_nxt;
+        ok_cur = ok_nxt;
+        bad_cur = bad_nxt;
       }
     } else if (warp == 1) {
       // ------------------------------------------------------------- MMA issuer ---------
@@ -228,7 +271,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       const uint32_t id_pv = idesc_bf16_f32(128, 128, true);
       const uint32_t q_addr = smem_u32(smem + pf::kQ);
       auto issue_s = [&](int j) -> bool {
-        const uint32_t g = tc + j, st = g % pf::kStages, b = g & 1u;
+        const uint32_t g = tc + j, st = g % pf::kStages, b = g % pf::kSBufs;
         if (!wait(&ctl->k_full[st], (g / pf::kStages) & 1u)) return false;
         tc_fence_after();
         if (lane == 0) {
@@ -247,10 +290,9 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       };
       bool ok = wait(&ctl->q_full, ic & 1u);
       if (ok) tc_fence_after();
-      if (ok) ok = issue_s(0);
-      if (ok && I.nkv > 1) ok = issue_s(1);
+      for (int j = 0; ok && j < min(pf::kSBufs, I.nkv); ++j) ok = issue_s(j);
       for (int j = 0; ok && j < I.nkv; ++j) {
-        const uint32_t g = tc + j, st = g % pf::kStages, b = g & 1u;
+        const uint32_t g = tc + j, st = g % pf::kStages, b = g % pf::kSBufs;
         if (!(ok = wait(&ctl->v_full[st], (g / pf::kStages) & 1u))) break;
         uint8_t* vt = smem + pf::kV + st * pf::kTile;
         const int zf = ctl->v_zero_from[st];
@@ -266,7 +308,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
         }
-        if (!(ok = wait(&ctl->p_full[b], (g >> 1) & 1u))) break;
+        if (!(ok = wait(&ctl->p_full[b], (g / pf::kSBufs) & 1u))) break;
         tc_fence_after();
         if (lane == 0) {
           const uint32_t v_addr = smem_u32(vt);
@@ -284,9 +326,9 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           tc_commit(&ctl->v_empty[st]);
         }
         __syncwarp();
-        // S of tile j+2 reuses this tile's S/P buffer: it is issued after (and runs after) the
+        // S of tile j+3 reuses this tile's S/P buffer: it is issued after (and runs after) the
         // P V that reads P from it
-        if (j + 2 < I.nkv) ok = issue_s(j + 2);
+        if (j + pf::kSBufs < I.nkv) ok = issue_s(j + pf::kSBufs);
       }
     } else {
       // ------------------------------------------------------------- softmax rows -------
@@ -299,8 +341,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       float m_used = 0.f, l = 0.f;
       bool ok = true;
       for (int j = 0; j < I.nkv; ++j) {
-        const uint32_t g = tc + j, b = g & 1u;
-        if (!(ok = wait(&ctl->s_full[b], (g >> 1) & 1u))) break;
+        const uint32_t g = tc + j, b = g % pf::kSBufs;
+        if (!(ok = wait(&ctl->s_full[b], (g / pf::kSBufs) & 1u))) break;
         tc_fence_after();
         const int kmax = row_ok ? row_pos - j * pf::kKeys : -1;  // keys 0..kmax are visible
         uint32_t sv[128];
@@ -361,7 +403,9 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         l = l * alpha + rs;
         if (__any_sync(0xffffffffu, rescale)) {
           // O may be rescaled only once the previous P V has landed in it
-          if (j > 0 && !(ok = wait(&ctl->o_done[(g - 1) & 1u], ((g - 1) >> 1) & 1u))) break;
+          if (j > 0 &&
+              !(ok = wait(&ctl->o_done[(g - 1) % pf::kSBufs], ((g - 1) / pf::kSBufs) & 1u)))
+            break;
           tc_fence_after();
           uint32_t o[128];
 #pragma unroll
@@ -381,7 +425,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       }
       // epilogue: O / l
       const uint32_t g_last = tc + I.nkv - 1;
-      if (ok && wait(&ctl->o_done[g_last & 1u], (g_last >> 1) & 1u)) {
+      if (ok && wait(&ctl->o_done[g_last % pf::kSBufs], (g_last / pf::kSBufs) & 1u)) {
         tc_fence_after();
         const float inv = (row_ok && l > 0.f) ? 1.f / l : 0.f;
         const int64_t orow = static_cast<int64_t>(I.t0 + tok) * p.num_q_heads + I.h * G + r % G;
