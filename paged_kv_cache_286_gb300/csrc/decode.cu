@@ -414,22 +414,30 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
         float mloc = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
         mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
         mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
-        const float m_new = fmaxf(m_run, mloc);
-        const float m_use = (m_new == -CUDART_INF_F) ? 0.f : m_new;
-        const float alpha = fast_exp2(m_run - m_use);
+        // Lazy rescale: the exponent base m_run moves only when a row's max exceeds it by more
+        // than 2^8 (p stays <= 256, exact in the P formats used); the final division uses the
+        // same base, so the result is unchanged.
+        const bool grow = mloc > m_run + kLazyRescaleLog2;
+        float alpha = 1.f;
+        if (grow) {
+          alpha = (m_run == -CUDART_INF_F) ? 0.f : fast_exp2(m_run - mloc);
+          m_run = mloc;
+        }
+        const float m_use = (m_run == -CUDART_INF_F) ? 0.f : m_run;
         float pr[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) pr[i] = fast_exp2(sv[i] - m_use);
         l_run = l_run * alpha + (pr[0] + pr[1]) + (pr[2] + pr[3]);
-        m_run = m_new;
-        const float alpha_a = __shfl_sync(0xffffffffu, alpha, 8 * qc);
-        const float alpha_b = __shfl_sync(0xffffffffu, alpha, 8 * qc + 4);
+        if (__any_sync(0xffffffffu, grow)) {
+          const float alpha_a = __shfl_sync(0xffffffffu, alpha, 8 * qc);
+          const float alpha_b = __shfl_sync(0xffffffffu, alpha, 8 * qc + 4);
 #pragma unroll
-        for (int j = 0; j < C::kKSteps; ++j) {
-          oacc[j][0] *= alpha_a;
-          oacc[j][1] *= alpha_b;
-          oacc[j][2] *= alpha_a;
-          oacc[j][3] *= alpha_b;
+          for (int j = 0; j < C::kKSteps; ++j) {
+            oacc[j][0] *= alpha_a;
+            oacc[j][1] *= alpha_b;
+            oacc[j][2] *= alpha_a;
+            oacc[j][3] *= alpha_b;
+          }
         }
 
         // keys past the tile's last position hold stale slots: zero their V (may be NaN)
@@ -457,10 +465,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                                   (((chunk & 7) ^ (vrow & 7)) << 4);
             uint32_t a[4];
             ldsm_x4_t(addr, a[0], a[1], a[2], a[3]);
-            a[0] &= vm_lo;
-            a[1] &= vm_lo;
-            a[2] &= vm_hi;
-            a[3] &= vm_hi;
+            if (nvalid < kBlockSize) {
+              a[0] &= vm_lo;
+              a[1] &= vm_lo;
+              a[2] &= vm_hi;
+              a[3] &= vm_hi;
+            }
             mma_bf16(oacc[j], a, ph0, ph1);
             mma_bf16(oacc[j], a, pl0, pl1);
           }
@@ -474,10 +484,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
             const uint32_t addr = vbase + vrow * 128 + (((chunk & 7) ^ (vrow & 7)) << 4);
             uint32_t r[4];  // (keys 0-7, chunk 2jj), (8-15, 2jj), (0-7, 2jj+1), (8-15, 2jj+1)
             ldsm_x4_t(addr, r[0], r[1], r[2], r[3]);
-            r[0] &= vm_lo;
-            r[1] &= vm_hi;
-            r[2] &= vm_lo;
-            r[3] &= vm_hi;
+            if (nvalid < kBlockSize) {
+              r[0] &= vm_lo;
+              r[1] &= vm_hi;
+              r[2] &= vm_lo;
+              r[3] &= vm_hi;
+            }
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
               // bytes (b0, b2) -> keys 2qc, 2qc+1 at d 2u; (b1, b3) -> the same keys at d 2u+1
@@ -688,7 +700,11 @@ cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const CUtens
   p.num_blocks = a.cache.num_blocks;
   p.max_context_len = a.max_context_len;
   p.max_query_len = a.max_query_len;
-  p.pblk = ws.pblk;
+  // An E4M3 block is half the bytes of a bf16 one: give E4M3 items twice the blocks (the
+  // workspace, sized for the bf16 choice, then holds fewer partitions than it has room for;
+  // pmax stays the row stride of the partial arrays).
+  const bool fp8_cache = a.cache.cache_dtype == PA_FP8_E4M3;
+  p.pblk = (fp8_cache && ws.pblk <= 32) ? ws.pblk * 2 : ws.pblk;
   p.pmax = ws.pmax;
   const bool prefill = qmap != nullptr && prefill_path_enabled(a.cache, a.num_q_heads,
                                                                a.num_kv_heads);

@@ -26,6 +26,7 @@ constexpr int kBlockSize = 16;            // tokens per physical block
 constexpr int kDecodeWarps = 4;           // warps per decode CTA
 constexpr int kRowsPerTile = 8;           // (query token x GQA head) rows per decode item
 constexpr int kDecodeMaxQuery = 16;       // sequences with n_s above this use the prefill path
+constexpr float kLazyRescaleLog2 = 8.f;  // softmax base moves only past 2^8 growth
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per bounded wait
 
 __device__ __forceinline__ void set_error(uint32_t* err, uint32_t bits) {
