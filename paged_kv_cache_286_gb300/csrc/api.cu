@@ -157,6 +157,37 @@ WsLayout workspace_layout(int32_t S, int32_t T, int32_t Hq, int32_t Hkv, int32_t
   return w;
 }
 
+cudaError_t launch_info_impl(const void* kern, int threads, int smem_bytes, LaunchInfo* out) {
+  struct Entry {
+    const void* kern;
+    int dev;
+    LaunchInfo info;
+  };
+  static std::mutex mu;
+  static Entry table[64];
+  static int used = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (table[i].kern == kern && table[i].dev == dev) {
+      *out = table[i].info;
+      return cudaSuccess;
+    }
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e != cudaSuccess) return e;
+  LaunchInfo li;
+  e = cudaDeviceGetAttribute(&li.sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&li.per_sm, kern, threads, smem_bytes);
+  if (e != cudaSuccess) return e;
+  if (li.per_sm < 1) li.per_sm = 1;
+  if (used < 64) table[used++] = Entry{kern, dev, li};
+  *out = li;
+  return cudaSuccess;
+}
+
 // Lets other translation units of the library report a host-side error through
 // pa_last_error_string.
 void set_last_error(const char* msg) { g_last_error = msg; }

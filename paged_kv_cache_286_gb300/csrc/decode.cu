@@ -645,13 +645,10 @@ static cudaError_t run_decode(const AttnArgs& a, const WsLayout& ws, const Decod
                               cudaEvent_t before, cudaEvent_t after) {
   constexpr int smem = decode_smem_bytes<D, kFp8, NST>();
   auto kern = decode_kernel<D, kFp8, NST>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  LaunchInfo li;
+  cudaError_t e = launch_info(kern, kDecodeWarps * 32, smem, &li);
   if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0, per_sm = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecodeWarps * 32, smem);
-  if (per_sm < 1) per_sm = 1;
+  const int sms = li.sms, per_sm = li.per_sm;
   const int tpt = kRowsPerTile / p.group;
   const int64_t qtiles_max = (std::min(a.max_query_len, p.decode_max_query) + tpt - 1) / tpt;
   const int64_t upper = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads * qtiles_max * ws.pmax;

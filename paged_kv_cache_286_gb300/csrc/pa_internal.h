@@ -10,6 +10,22 @@
 
 namespace pa {
 
+// Per-device launch facts of one kernel (SM count, resident CTAs per SM), with its dynamic
+// shared-memory limit raised once per device: computed on first use and cached.
+struct LaunchInfo {
+  int sms = 0;
+  int per_sm = 0;
+};
+
+// Cached per (kernel address, device): the function's C++ type is shared by every
+// instantiation of a kernel template, so the key must be the address.
+cudaError_t launch_info_impl(const void* kern, int threads, int smem_bytes, LaunchInfo* out);
+
+template <typename Kernel>
+cudaError_t launch_info(Kernel kern, int threads, int smem_bytes, LaunchInfo* out) {
+  return launch_info_impl(reinterpret_cast<const void*>(kern), threads, smem_bytes, out);
+}
+
 // Everything pa_attention received, after host validation.
 struct AttnArgs {
   const void* q;

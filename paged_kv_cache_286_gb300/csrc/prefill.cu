@@ -491,12 +491,10 @@ cudaError_t launch_prefill(const AttnArgs& a, const int32_t* item_start, WsHeade
   p.num_blocks = a.cache.num_blocks;
   p.out_bf16 = a.out_dtype == PA_BF16;
   p.score_log2 = a.scale * 1.4426950408889634f;
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       pf::kSmem);
+  LaunchInfo li;
+  cudaError_t e = launch_info(prefill_kernel, pf::kThreads, pf::kSmem, &li);
   if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = li.sms;
   const int G = p.group;
   const int64_t upper =
       static_cast<int64_t>(a.num_kv_heads) *
