@@ -89,8 +89,8 @@ typedef struct {
  * to pa_cache_append needs at least this many bytes (pa_attention's workspace qualifies). */
 #define PA_WORKSPACE_HEADER_BYTES 256
 
-/* Device error-word bits (returned by pa_check_error through its status; the raw word is
- * available through pa_check_error_word). */
+/* Device error-word bits (pa_check_error maps them to its status and returns the raw word
+ * through its word_out argument). */
 #define PA_DEVERR_BLOCK_ID 0x1u    /* block table entry outside [0, num_blocks) */
 #define PA_DEVERR_SLOT 0x2u        /* slot >= num_blocks * block_size */
 #define PA_DEVERR_LENGTHS 0x4u     /* n_s < 0, n_s > context_len, or a host hint exceeded */
@@ -108,6 +108,20 @@ typedef struct {
 pa_status pa_cache_append(const void* k, const void* v, const int64_t* slot_mapping,
                           int32_t num_tokens, void* k_cache, void* v_cache,
                           const pa_cache_desc* cache, void* workspace, cudaStream_t stream);
+
+/* Copy whole blocks inside the pool: for each pair i, block block_pairs[2i] (source) is copied
+ * to block block_pairs[2i+1] (destination), all kv heads, K and V, bit for bit.
+ * "Serving LLMs with vLLM: Continuous Batching and PagedAttention Explained", section
+ * "Copy-on-Write": before a sequence writes into a shared block, the engine copies it to a
+ * fresh block and points only that sequence's table at the copy.
+ *   block_pairs  [num_pairs][2] int32 (device); num_pairs <= 65535.
+ *   workspace    >= PA_WORKSPACE_HEADER_BYTES bytes (device); a block id outside the pool sets
+ *                PA_DEVERR_BLOCK_ID and that pair is skipped.
+ * Pairs must not overlap (no block is both a source and a destination, no destination twice);
+ * otherwise the result is undefined. */
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, const pa_cache_desc* cache,
+                         const int32_t* block_pairs, int32_t num_pairs, void* workspace,
+                         cudaStream_t stream);
 
 /* Workspace bytes pa_attention needs for a step of this shape (host-only, no device call).
  * max_context_len / max_query_len are upper bounds of context_lens[s] and n_s. */

@@ -20,7 +20,10 @@ STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED",
 
 EXPORTED = ["pa_cache_append", "pa_attention_workspace_size", "pa_attention", "pa_check_error",
             "pa_workspace_init", "pa_last_error_string", "pa_version",
-            "pa_set_kernel_timing_events", "pa_attention_noalloc"]
+            "pa_set_kernel_timing_events", "pa_attention_noalloc", "pa_copy_blocks"]
+EXPORTED_BM = ["pa_bm_create", "pa_bm_destroy", "pa_bm_num_free", "pa_bm_append",
+               "pa_bm_append_tokens", "pa_bm_fork", "pa_bm_free", "pa_bm_block_table",
+               "pa_bm_num_tokens", "pa_bm_refcount", "pa_bm_cached_prefix"]
 
 
 class CacheDesc(ctypes.Structure):
@@ -62,6 +65,31 @@ def load() -> ctypes.CDLL:
                                        i32p, i32p, i32, i32, i32, i32, i32, i32, ctypes.c_float,
                                        vp, i32, vp, vp]
     L.pa_attention_noalloc.restype = ctypes.c_int
+    L.pa_copy_blocks.argtypes = [vp, vp, ctypes.POINTER(CacheDesc), vp, i32, vp, vp]
+    L.pa_copy_blocks.restype = ctypes.c_int
+    i64 = ctypes.c_int64
+    L.pa_bm_create.argtypes = [i32, i32]
+    L.pa_bm_create.restype = vp
+    L.pa_bm_destroy.argtypes = [vp]
+    L.pa_bm_destroy.restype = None
+    L.pa_bm_num_free.argtypes = [vp]
+    L.pa_bm_num_free.restype = i32
+    L.pa_bm_append.argtypes = [vp, i64, i32, vp, vp, i32]
+    L.pa_bm_append.restype = i32
+    L.pa_bm_append_tokens.argtypes = [vp, i64, vp, i32, vp, vp, i32, vp]
+    L.pa_bm_append_tokens.restype = i32
+    L.pa_bm_cached_prefix.argtypes = [vp, vp, i32]
+    L.pa_bm_cached_prefix.restype = i32
+    L.pa_bm_fork.argtypes = [vp, i64, i64]
+    L.pa_bm_fork.restype = i32
+    L.pa_bm_free.argtypes = [vp, i64]
+    L.pa_bm_free.restype = i32
+    L.pa_bm_block_table.argtypes = [vp, i64, vp, i32]
+    L.pa_bm_block_table.restype = i32
+    L.pa_bm_num_tokens.argtypes = [vp, i64]
+    L.pa_bm_num_tokens.restype = i64
+    L.pa_bm_refcount.argtypes = [vp, i32]
+    L.pa_bm_refcount.restype = i32
     L.pa_check_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
     L.pa_check_error.restype = ctypes.c_int
     L.pa_workspace_init.argtypes = [vp, vp]

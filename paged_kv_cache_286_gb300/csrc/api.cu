@@ -250,6 +250,26 @@ pa_status pa_cache_append(const void* k, const void* v, const int64_t* slot_mapp
   return PA_OK;
 }
 
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, const pa_cache_desc* cache,
+                         const int32_t* block_pairs, int32_t num_pairs, void* workspace,
+                         cudaStream_t stream) {
+  g_last_error.clear();
+  if (num_pairs < 0 || num_pairs > 65535)
+    return fail(PA_ERR_INVALID_ARG, "num_pairs must be in [0, 65535]");
+  pa_status st = check_cache_desc(cache, false);
+  if (st != PA_OK) return st;
+  if (!workspace) return fail(PA_ERR_INVALID_ARG, "workspace is NULL");
+  if (num_pairs == 0) return PA_OK;
+  if (!k_cache || !v_cache || !block_pairs) return fail(PA_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(block_pairs, 4) ||
+      !aligned(workspace, 4))
+    return fail(PA_ERR_INVALID_ARG, "misaligned pointer (caches need 16 bytes)");
+  cudaError_t e = pa::launch_copy_blocks(k_cache, v_cache, *cache, block_pairs, num_pairs,
+                                         static_cast<uint32_t*>(workspace), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "pa_copy_blocks launch");
+  return PA_OK;
+}
+
 size_t pa_attention_workspace_size(int32_t num_seqs, int32_t num_q_tokens, int32_t num_q_heads,
                                    int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                                    int32_t max_context_len, int32_t max_query_len) {

@@ -72,6 +72,10 @@ cudaError_t launch_cache_append(const void* k, const void* v, const int64_t* slo
 
 void set_last_error(const char* msg);
 
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const pa_cache_desc& c,
+                               const int32_t* pairs, int32_t num_pairs, uint32_t* err,
+                               cudaStream_t stream);
+
 // True when chunks with more than kDecodeMaxQuery queries run on the tcgen05 tile kernel
 // (bf16 pool, head_dim 128, GQA group dividing 128); otherwise every sequence takes the
 // split-KV kernel.

@@ -43,6 +43,26 @@ def test_library_exports_every_declared_function(lib):
         assert hasattr(lib, n)
 
 
+def test_block_manager_header_is_exported(lib):
+    text = open(os.path.join(ROOT, "include", "pa_block_manager.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = sorted(set(re.findall(r"\b(pa_bm_[a-z_0-9]+)\s*\(", text)))
+    from paged_kv_cache_286_gb300 import _lib
+    assert names == sorted(_lib.EXPORTED_BM)
+    out = subprocess.run(["nm", "-D", "--defined-only", pa_build.LIB], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (pa_bm_[a-z_0-9]+)$", out, flags=re.M))
+    assert set(names) <= exported
+
+
+def test_copy_blocks_rejects_bad_arguments(lib):
+    d = _desc()
+    assert lib.pa_copy_blocks(FAKE, FAKE, ctypes.byref(d), FAKE, -1, FAKE, None) == 1
+    assert lib.pa_copy_blocks(FAKE, FAKE, ctypes.byref(d), FAKE, 70000, FAKE, None) == 1
+    assert lib.pa_copy_blocks(FAKE, FAKE, ctypes.byref(d), None, 3, FAKE, None) == 1
+    assert lib.pa_copy_blocks(FAKE, FAKE, ctypes.byref(d), FAKE, 0, FAKE, None) == 0
+
+
 def test_binding_lists_every_export():
     from paged_kv_cache_286_gb300 import _lib
     assert sorted(_lib.EXPORTED) == header_functions()
