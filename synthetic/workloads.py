@@ -40,6 +40,8 @@ CONFIG_NAMES = {
        "(512 new, no prefix) and (512 new after a 2048-token prefix), bf16 KV",
     5: "long-context decode, shared prefix: Hq=32, Hkv=8, D=128, bs=16, 16 seqs at 32768 "
        "tokens sharing a 1504-token (94-block) prefix, bf16 KV",
+    6: "speculative verify step: Hq=32, Hkv=8, D=128, bs=16, 64 seqs with contexts U[512,4096], "
+       "5 causal query tokens each (1 accepted + 4 draft), bf16 KV",
 }
 
 _CHUNK = 1 << 24  # elements per generator draw; fixed so that draws are reproducible
@@ -282,6 +284,9 @@ def config_lengths(config_id: int):
     if config_id == 5:
         return [32768] * 16, [1] * 16, dict(num_q_heads=32, num_kv_heads=8, head_dim=128,
                                             shared_prefix_blocks=94)
+    if config_id == 6:
+        ctx = rng.integers(512, 4096, size=64, endpoint=True)
+        return ctx.tolist(), [5] * 64, dict(num_q_heads=32, num_kv_heads=8, head_dim=128)
     raise ValueError(f"no workload {config_id}")
 
 

@@ -286,3 +286,9 @@ def test_config4_full_size_sampled():
 @pytest.mark.slow
 def test_config5_full_size_sampled():
     _sampled(5, 2)
+
+
+@pytest.mark.slow
+def test_speculative_verify_workload_sampled():
+    """Multi-query verify step (1 accepted + 4 draft tokens per sequence, causal among them)."""
+    _sampled(6, 6)
