@@ -48,7 +48,8 @@
  *   query_start_loc [num_seqs + 1] int32: exclusive prefix sum of per-sequence query counts
  *                n_s, starting at 0.  The n_s queries of sequence s are its last n_s positions
  *                p_i = context_len - n_s + i, and query i attends keys 0..p_i.
- *   GQA:         q head h reads kv head h / (num_q_heads / num_kv_heads).
+ *   GQA:         q head h reads kv head h / (num_q_heads / num_kv_heads); groups of up to 16
+ *                q heads per kv head are built.
  */
 #ifndef PAGED_KV_PA_H_
 #define PAGED_KV_PA_H_

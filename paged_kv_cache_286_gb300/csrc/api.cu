@@ -296,8 +296,8 @@ pa_status pa_attention(const void* q, int32_t num_q_tokens, const void* k_cache,
   if (num_q_heads % num_kv_heads != 0)
     return fail(PA_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d",
                 num_q_heads, num_kv_heads);
-  if (num_q_heads / num_kv_heads > pa::kRowsPerTile)
-    return fail(PA_ERR_UNSUPPORTED, "GQA group of %d q heads per kv head is not built (<= 8)",
+  if (num_q_heads / num_kv_heads > pa::kDecodeMaxGroup)
+    return fail(PA_ERR_UNSUPPORTED, "GQA group of %d q heads per kv head is not built (<= 16)",
                 num_q_heads / num_kv_heads);
   if (head_dim != cache->head_dim || num_kv_heads != cache->num_kv_heads)
     return fail(PA_ERR_INVALID_ARG, "head_dim / num_kv_heads disagree with the cache descriptor");

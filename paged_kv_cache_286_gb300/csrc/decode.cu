@@ -6,16 +6,18 @@
 // key/value j live in physical block block_tables[s][j / 16] at offset j % 16.
 //
 // Design (GB300 / sm_103a):
-//  * Work item = (sequence, kv head, tile of 8 rows, KV partition of `pblk` blocks).  A row is a
-//    (query token, q head of the GQA group) pair, so one item loads each K/V block once for the
-//    whole group.  A plan kernel turns context lengths into per-sequence item counts; the
+//  * Work item = (sequence, kv head, tile of 8 or 16 rows, KV partition of `pblk` blocks).  A row
+//    is a (query token, q head of the GQA group) pair, so one item loads each K/V block once for
+//    the whole group and for as many of the sequence's query tokens as the tile holds.  16-row
+//    tiles (both halves of the MMA's M) serve groups above 8 and multi-token runs (speculative
+//    verify, short chunks); single-token decode keeps 8-row tiles, the cheaper instance.  A plan kernel turns context lengths into per-sequence item counts; the
 //    attention kernel is persistent and takes items from an atomic counter.
 //  * Each of the CTA's 4 warps owns every 4th block of the partition and streams it through its
 //    own ring of shared-memory stages: one lane issues 2-D TMA tile copies of the (block, head)
 //    K and V tiles (128-byte swizzle) after reading the block id from the table, completion is
 //    counted on the stage's mbarrier.  The HBM stream is the whole cost of decode.
-//  * Scores and P.V run on warp-level tensor-core MMAs (m16n8k16): S = Q K^T with the 8 rows as
-//    M (padded to 16), and O^T = V^T P^T so that the probabilities feed the second MMA straight
+//  * Scores and P.V run on warp-level tensor-core MMAs (m16n8k16): S = Q K^T with the rows as M
+//    (an 8-row tile pads M to 16), and O^T = V^T P^T so that the probabilities feed the second MMA straight
 //    from the first one's accumulators.  bf16 caches: P is split into bf16 hi + lo parts, which
 //    keeps P exact to ~2^-16.  E4M3 caches: K and V are converted to f16 in registers (exact),
 //    q is scaled by a power of two per row into f16 range, P is f16.
@@ -53,6 +55,7 @@ struct DecodeParams {
   int32_t pblk;
   int32_t pmax;
   int32_t decode_max_query;
+  int32_t rows_per_tile;   // 8 * RT of the decode kernel instance
   int32_t out_bf16;
   float score_log2;        // scale * log2(e) (* k_scale for E4M3)
   float v_out_scale;       // v_scale for E4M3, else 1
@@ -73,7 +76,7 @@ __device__ __forceinline__ int decode_items_of(const DecodeParams& p, int n, int
     return 0;
   }
   if (n > p.decode_max_query) return 0;
-  const int tpt = kRowsPerTile / p.group;  // query tokens per tile
+  const int tpt = p.rows_per_tile / p.group;  // query tokens per tile
   const int qtiles = ceil_div(n, tpt);
   const int nparts = ceil_div(ceil_div(L, kBlockSize), p.pblk);
   return p.num_kv_heads * qtiles * nparts;
@@ -174,12 +177,14 @@ struct ItemInfo {
   int s, h, qt, part, t0, n, L, nparts, blk_begin, blk_end, pos_base, rows, valid;
 };
 
-template <int D, bool kFp8, int NST>
+template <int D, bool kFp8, int NST, int RT>
 __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     decode_kernel(const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
+  // RT row tiles of 8 rows: rows quad and quad + 8 of the m16 MMA (RT = 2 uses both halves)
   using C = DecodeCfg<D, kFp8>;
-  static_assert(C::kStageBytes * NST >= kRowsPerTile * D * 4 + 2 * kRowsPerTile * 4,
+  constexpr int R = 8 * RT;
+  static_assert(C::kStageBytes * NST >= 16 * D * 4 + 2 * 16 * 4,
                 "merge scratch must fit in a warp's stage buffers");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -221,7 +226,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
         const int t0 = p.qsl[s];
         const int n = p.qsl[s + 1] - t0;
         const int L = p.context_lens[s];
-        const int tpt = kRowsPerTile / p.group;
+        const int tpt = R / p.group;
         const int qtiles = ceil_div(n, tpt);
         const int nblk = ceil_div(L, kBlockSize);
         const int nparts = ceil_div(nblk, p.pblk);
@@ -248,11 +253,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     if (!I.valid || any_timeout) break;
     const uint32_t it0 = it;  // blocks consumed before this item
 
-    // ---- rows held by this lane: S row `quad`; O^T columns 2*qc, 2*qc+1 ------------------
-    const int row = quad;
-    const bool row_ok = row < I.rows;
-    const int row_tok = row_ok ? row / p.group : 0;
-    const int row_pos = I.pos_base + row_tok;
+    // ---- rows held by this lane: S rows quad + 8r; O^T columns 2qc, 2qc+1 of each tile --
+    bool row_ok[RT];
+    int row_tok[RT], row_pos[RT];
+#pragma unroll
+    for (int r = 0; r < RT; ++r) {
+      const int row = quad + 8 * r;
+      row_ok[r] = row < I.rows;
+      row_tok[r] = row_ok[r] ? row / p.group : 0;
+      row_pos[r] = I.pos_base + row_tok[r];
+    }
     const int pos_last = I.pos_base + I.n - 1;
 
     // ---- table entries of this warp's blocks, one per lane -----------------------------
@@ -292,22 +302,24 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     const int npre = min(NST, nb_w);
     for (int k = 0; k < npre; ++k) issue(k);
 
-    // ---- q fragments (A operand of S = Q K^T), rows 8..15 are zero -----------------------
-    uint32_t qa[C::kKSteps][2];
-    float row_scale = p.score_log2;
-    {
+    // ---- q fragments (A operand of S = Q K^T): a0/a2 row quad, a1/a3 row quad + 8 -------
+    uint32_t qa[C::kKSteps][4];
+    float row_scale[RT];
+#pragma unroll
+    for (int ks = 0; ks < C::kKSteps; ++ks) qa[ks][1] = qa[ks][3] = 0u;  // rows 8..15 (RT = 1)
+#pragma unroll
+    for (int r = 0; r < RT; ++r) {
+      const int row = quad + 8 * r;
       const __nv_bfloat16* qrow =
-          p.q + (static_cast<int64_t>(I.t0 + row_tok) * p.num_q_heads + I.h * p.group +
-                 (row_ok ? row % p.group : 0)) * D;
+          p.q + (static_cast<int64_t>(I.t0 + row_tok[r]) * p.num_q_heads + I.h * p.group +
+                 (row_ok[r] ? row % p.group : 0)) * D;
       if constexpr (!kFp8) {
+        row_scale[r] = p.score_log2;
 #pragma unroll
         for (int ks = 0; ks < C::kKSteps; ++ks) {
-          if (row_ok) {
-            qa[ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * qc));
-            qa[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * qc));
-          } else {
-            qa[ks][0] = qa[ks][1] = 0u;
-          }
+          const uint32_t* src = reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * qc);
+          qa[ks][r] = row_ok[r] ? __ldg(src) : 0u;
+          qa[ks][2 + r] = row_ok[r] ? __ldg(src + 4) : 0u;
         }
       } else {
         // k index 2c,2c+1 of a k-step <-> d 4c,4c+1; k index 2c+8,2c+9 <-> d 4c+2,4c+3
@@ -315,8 +327,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
         float amax = 0.f;
 #pragma unroll
         for (int ks = 0; ks < C::kKSteps; ++ks) {
-          raw[ks] = row_ok ? __ldg(reinterpret_cast<const uint2*>(qrow + 16 * ks + 4 * qc))
-                           : make_uint2(0u, 0u);
+          raw[ks] = row_ok[r] ? __ldg(reinterpret_cast<const uint2*>(qrow + 16 * ks + 4 * qc))
+                              : make_uint2(0u, 0u);
           amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16lo_to_f32(raw[ks].x)),
                                          fabsf(bf16hi_to_f32(raw[ks].x))),
                                    fmaxf(fabsf(bf16lo_to_f32(raw[ks].y)),
@@ -329,20 +341,26 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
         if (amax > 0.f) frexpf(amax, &ex);
         const int e = max(-100, min(100, 15 - ex));
         const float up = ldexpf(1.f, e);
-        row_scale = p.score_log2 * ldexpf(1.f, -e);
+        row_scale[r] = p.score_log2 * ldexpf(1.f, -e);
 #pragma unroll
         for (int ks = 0; ks < C::kKSteps; ++ks) {
-          qa[ks][0] = pack_f16x2(bf16lo_to_f32(raw[ks].x) * up, bf16hi_to_f32(raw[ks].x) * up);
-          qa[ks][1] = pack_f16x2(bf16lo_to_f32(raw[ks].y) * up, bf16hi_to_f32(raw[ks].y) * up);
+          qa[ks][r] = pack_f16x2(bf16lo_to_f32(raw[ks].x) * up, bf16hi_to_f32(raw[ks].x) * up);
+          qa[ks][2 + r] =
+              pack_f16x2(bf16lo_to_f32(raw[ks].y) * up, bf16hi_to_f32(raw[ks].y) * up);
         }
       }
     }
 
-    float m_run = -CUDART_INF_F;  // running max of row `quad`, log2 domain
-    float l_run = 0.f;            // this lane's share of the running sum
-    float oacc[C::kKSteps][4];
+    float m_run[RT], l_run[RT];  // running max (log2 domain) and this lane's share of the sum
+    float oacc[RT][C::kKSteps][4];
 #pragma unroll
-    for (int j = 0; j < C::kKSteps; ++j) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.f;
+    for (int r = 0; r < RT; ++r) {
+      m_run[r] = -CUDART_INF_F;
+      l_run[r] = 0.f;
+#pragma unroll
+      for (int j = 0; j < C::kKSteps; ++j)
+        oacc[r][j][0] = oacc[r][j][1] = oacc[r][j][2] = oacc[r][j][3] = 0.f;
+    }
 
     for (int k = 0; k < nb_w; ++k) {
       const uint32_t st = it % NST;
@@ -377,66 +395,23 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                                     (((chunk & 7) ^ (krow & 7)) << 4);
               uint32_t b0, b1, b2, b3;
               ldsm_x4(addr, b0, b1, b2, b3);
-              const uint32_t a0[4] = {qa[2 * kk][0], 0u, qa[2 * kk][1], 0u};
-              const uint32_t a1[4] = {qa[2 * kk + 1][0], 0u, qa[2 * kk + 1][1], 0u};
-              mma_bf16(sacc[nt], a0, b0, b1);
-              mma_bf16(sacc[nt], a1, b2, b3);
+              mma_bf16(sacc[nt], qa[2 * kk], b0, b1);
+              mma_bf16(sacc[nt], qa[2 * kk + 1], b2, b3);
             }
           } else {
 #pragma unroll
             for (int kk = 0; kk < D / 64; ++kk) {
               const int chunk = 4 * kk + (lane >> 3);  // 16-byte chunk = 16 d = one k-step
               const uint32_t addr = kbase + krow * 128 + (((chunk & 7) ^ (krow & 7)) << 4);
-              uint32_t r[4];
-              ldsm_x4(addr, r[0], r[1], r[2], r[3]);
+              uint32_t rr[4];
+              ldsm_x4(addr, rr[0], rr[1], rr[2], rr[3]);
 #pragma unroll
               for (int m = 0; m < 4; ++m) {
-                const int ks = 4 * kk + m;
-                const uint32_t a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
                 uint32_t b0, b1;
-                e4m3x4_to_f16x2x2(r[m], b0, b1);
-                mma_f16(sacc[nt], a, b0, b1);
+                e4m3x4_to_f16x2x2(rr[m], b0, b1);
+                mma_f16(sacc[nt], qa[4 * kk + m], b0, b1);
               }
             }
-          }
-        }
-
-        // ---- online softmax for row `quad` over keys 8nt + 2qc + e ----------------------
-        float sv[4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int kidx = key0 + 8 * nt + 2 * qc + e;
-            const bool ok = row_ok && kidx <= row_pos;
-            sv[2 * nt + e] = ok ? sacc[nt][e] * row_scale : -CUDART_INF_F;
-          }
-        float mloc = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
-        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
-        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
-        // Lazy rescale: the exponent base m_run moves only when a row's max exceeds it by more
-        // than 2^8 (p stays <= 256, exact in the P formats used); the final division uses the
-        // same base, so the result is unchanged.
-        const bool grow = mloc > m_run + kLazyRescaleLog2;
-        float alpha = 1.f;
-        if (grow) {
-          alpha = (m_run == -CUDART_INF_F) ? 0.f : fast_exp2(m_run - mloc);
-          m_run = mloc;
-        }
-        const float m_use = (m_run == -CUDART_INF_F) ? 0.f : m_run;
-        float pr[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) pr[i] = fast_exp2(sv[i] - m_use);
-        l_run = l_run * alpha + (pr[0] + pr[1]) + (pr[2] + pr[3]);
-        if (__any_sync(0xffffffffu, grow)) {
-          const float alpha_a = __shfl_sync(0xffffffffu, alpha, 8 * qc);
-          const float alpha_b = __shfl_sync(0xffffffffu, alpha, 8 * qc + 4);
-#pragma unroll
-          for (int j = 0; j < C::kKSteps; ++j) {
-            oacc[j][0] *= alpha_a;
-            oacc[j][1] *= alpha_b;
-            oacc[j][2] *= alpha_a;
-            oacc[j][3] *= alpha_b;
           }
         }
 
@@ -449,14 +424,64 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                   (9 + 2 * qc < nvalid ? 0xffff0000u : 0u);
         }
 
-        // ---- O^T += V^T P^T --------------------------------------------------------------
+        // ---- online softmax for rows quad + 8r over keys 8nt + 2qc + e ------------------
+        uint32_t pb[RT][4];  // P^T fragments: bf16 hi pair 0, hi pair 1, lo 0, lo 1 (or f16)
+#pragma unroll
+        for (int r = 0; r < RT; ++r) {
+          float sv[4];
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int kidx = key0 + 8 * nt + 2 * qc + e;
+              const bool ok = row_ok[r] && kidx <= row_pos[r];
+              sv[2 * nt + e] = ok ? sacc[nt][2 * r + e] * row_scale[r] : -CUDART_INF_F;
+            }
+          float mloc = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+          mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
+          mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
+          // Lazy rescale: the exponent base m_run moves only when a row's max exceeds it by
+          // more than 2^8 (p stays <= 256, exact in the P formats used); the final division
+          // uses the same base, so the result is unchanged.
+          const bool grow = mloc > m_run[r] + kLazyRescaleLog2;
+          float alpha = 1.f;
+          if (grow) {
+            alpha = (m_run[r] == -CUDART_INF_F) ? 0.f : fast_exp2(m_run[r] - mloc);
+            m_run[r] = mloc;
+          }
+          const float m_use = (m_run[r] == -CUDART_INF_F) ? 0.f : m_run[r];
+          float pr[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) pr[i] = fast_exp2(sv[i] - m_use);
+          l_run[r] = l_run[r] * alpha + (pr[0] + pr[1]) + (pr[2] + pr[3]);
+          if (__any_sync(0xffffffffu, grow)) {
+            // O^T columns 2qc, 2qc+1 of tile r belong to rows 8r + 2qc (+1): held by lanes
+            // 8qc and 8qc + 4
+            const float alpha_a = __shfl_sync(0xffffffffu, alpha, 8 * qc);
+            const float alpha_b = __shfl_sync(0xffffffffu, alpha, 8 * qc + 4);
+#pragma unroll
+            for (int j = 0; j < C::kKSteps; ++j) {
+              oacc[r][j][0] *= alpha_a;
+              oacc[r][j][1] *= alpha_b;
+              oacc[r][j][2] *= alpha_a;
+              oacc[r][j][3] *= alpha_b;
+            }
+          }
+          if constexpr (!kFp8) {
+            pb[r][0] = pack_bf16x2(pr[0], pr[1]);
+            pb[r][1] = pack_bf16x2(pr[2], pr[3]);
+            pb[r][2] = pack_bf16x2(pr[0] - bf16lo_to_f32(pb[r][0]),
+                                   pr[1] - bf16hi_to_f32(pb[r][0]));
+            pb[r][3] = pack_bf16x2(pr[2] - bf16lo_to_f32(pb[r][1]),
+                                   pr[3] - bf16hi_to_f32(pb[r][1]));
+          } else {
+            pb[r][0] = pack_f16x2(pr[0], pr[1]);
+            pb[r][1] = pack_f16x2(pr[2], pr[3]);
+          }
+        }
+
+        // ---- O^T += V^T P^T (one V^T fragment feeds every row tile) ----------------------
         if constexpr (!kFp8) {
-          const uint32_t ph0 = pack_bf16x2(pr[0], pr[1]);
-          const uint32_t ph1 = pack_bf16x2(pr[2], pr[3]);
-          const uint32_t pl0 =
-              pack_bf16x2(pr[0] - bf16lo_to_f32(ph0), pr[1] - bf16hi_to_f32(ph0));
-          const uint32_t pl1 =
-              pack_bf16x2(pr[2] - bf16lo_to_f32(ph1), pr[3] - bf16hi_to_f32(ph1));
           const int vrow = ((lane >> 4) << 3) + (lane & 7);  // key row of this lane's address
 #pragma unroll
           for (int j = 0; j < C::kKSteps; ++j) {
@@ -471,32 +496,34 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
               a[2] &= vm_hi;
               a[3] &= vm_hi;
             }
-            mma_bf16(oacc[j], a, ph0, ph1);
-            mma_bf16(oacc[j], a, pl0, pl1);
+#pragma unroll
+            for (int r = 0; r < RT; ++r) {
+              mma_bf16(oacc[r][j], a, pb[r][0], pb[r][1]);
+              mma_bf16(oacc[r][j], a, pb[r][2], pb[r][3]);
+            }
           }
         } else {
-          const uint32_t pf0 = pack_f16x2(pr[0], pr[1]);
-          const uint32_t pf1 = pack_f16x2(pr[2], pr[3]);
           const int vrow = ((lane >> 3) & 1) * 8 + (lane & 7);
 #pragma unroll
           for (int jj = 0; jj < D / 32; ++jj) {
             const int chunk = 2 * jj + (lane >> 4);
             const uint32_t addr = vbase + vrow * 128 + (((chunk & 7) ^ (vrow & 7)) << 4);
-            uint32_t r[4];  // (keys 0-7, chunk 2jj), (8-15, 2jj), (0-7, 2jj+1), (8-15, 2jj+1)
-            ldsm_x4_t(addr, r[0], r[1], r[2], r[3]);
+            uint32_t rr[4];  // (keys 0-7, chunk 2jj), (8-15, 2jj), (0-7, 2jj+1), (8-15, 2jj+1)
+            ldsm_x4_t(addr, rr[0], rr[1], rr[2], rr[3]);
             if (nvalid < kBlockSize) {
-              r[0] &= vm_lo;
-              r[1] &= vm_hi;
-              r[2] &= vm_lo;
-              r[3] &= vm_hi;
+              rr[0] &= vm_lo;
+              rr[1] &= vm_hi;
+              rr[2] &= vm_lo;
+              rr[3] &= vm_hi;
             }
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
               // bytes (b0, b2) -> keys 2qc, 2qc+1 at d 2u; (b1, b3) -> the same keys at d 2u+1
               uint32_t a[4];
-              e4m3x4_to_f16x2x2(prmt(r[2 * h2], 0u, 0x3120u), a[0], a[1]);
-              e4m3x4_to_f16x2x2(prmt(r[2 * h2 + 1], 0u, 0x3120u), a[2], a[3]);
-              mma_f16(oacc[2 * jj + h2], a, pf0, pf1);
+              e4m3x4_to_f16x2x2(prmt(rr[2 * h2], 0u, 0x3120u), a[0], a[1]);
+              e4m3x4_to_f16x2x2(prmt(rr[2 * h2 + 1], 0u, 0x3120u), a[2], a[3]);
+#pragma unroll
+              for (int r = 0; r < RT; ++r) mma_f16(oacc[r][2 * jj + h2], a, pb[r][0], pb[r][1]);
             }
           }
         }
@@ -508,30 +535,34 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     if (timed_out) it = 0;  // results are void; phase tracking no longer matters
 
     // ---- per-warp state -> shared memory (this warp's own stage buffers) -----------------
-    float l_row = l_run;
-    l_row += __shfl_xor_sync(0xffffffffu, l_row, 1);
-    l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
-    float* so = reinterpret_cast<float*>(wbuf);           // [8][D]
-    float* sm = so + kRowsPerTile * D;                     // [8]
-    float* sl = sm + kRowsPerTile;                         // [8]
+    float* so = reinterpret_cast<float*>(wbuf);           // [16][D]
+    float* sm = so + 16 * D;                               // [16]
+    float* sl = sm + 16;                                   // [16]
 #pragma unroll
-    for (int j = 0; j < C::kKSteps; ++j) {
-      int da, db;
-      if constexpr (!kFp8) {
-        da = 16 * j + quad;
-        db = da + 8;
-      } else {
-        da = 16 * j + 2 * quad;
-        db = da + 1;
+    for (int r = 0; r < RT; ++r) {
+      float l_row = l_run[r];
+      l_row += __shfl_xor_sync(0xffffffffu, l_row, 1);
+      l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
+#pragma unroll
+      for (int j = 0; j < C::kKSteps; ++j) {
+        int da, db;
+        if constexpr (!kFp8) {
+          da = 16 * j + quad;
+          db = da + 8;
+        } else {
+          da = 16 * j + 2 * quad;
+          db = da + 1;
+        }
+        const int ra = 8 * r + 2 * qc;
+        so[ra * D + da] = oacc[r][j][0];
+        so[(ra + 1) * D + da] = oacc[r][j][1];
+        so[ra * D + db] = oacc[r][j][2];
+        so[(ra + 1) * D + db] = oacc[r][j][3];
       }
-      so[(2 * qc) * D + da] = oacc[j][0];
-      so[(2 * qc + 1) * D + da] = oacc[j][1];
-      so[(2 * qc) * D + db] = oacc[j][2];
-      so[(2 * qc + 1) * D + db] = oacc[j][3];
-    }
-    if (qc == 0) {
-      sm[quad] = m_run;
-      sl[quad] = l_row;
+      if (qc == 0) {
+        sm[quad + 8 * r] = m_run[r];
+        sl[quad + 8 * r] = l_row;
+      }
     }
     __syncthreads();
 
@@ -542,7 +573,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 #pragma unroll
       for (int w = 0; w < kDecodeWarps; ++w) {
         const float* wsm = reinterpret_cast<const float*>(smem + w * NST * C::kStageBytes) +
-                           kRowsPerTile * D;
+                           16 * D;
         M = fmaxf(M, wsm[r]);
       }
       float Lsum = 0.f, O = 0.f;
@@ -550,9 +581,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 #pragma unroll
         for (int w = 0; w < kDecodeWarps; ++w) {
           const float* wso = reinterpret_cast<const float*>(smem + w * NST * C::kStageBytes);
-          const float mw = wso[kRowsPerTile * D + r];
+          const float mw = wso[16 * D + r];
           const float f = fast_exp2(mw - M);
-          Lsum += wso[kRowsPerTile * D + kRowsPerTile + r] * f;
+          Lsum += wso[16 * D + 16 + r] * f;
           O += wso[r * D + d] * f;
         }
       }
@@ -639,17 +670,17 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p, int32_
   }
 }
 
-template <int D, bool kFp8, int NST>
+template <int D, bool kFp8, int NST, int RT>
 static cudaError_t run_decode(const AttnArgs& a, const WsLayout& ws, const DecodeParams& p,
                               const CUtensorMap& kmap, const CUtensorMap& vmap,
                               cudaEvent_t before, cudaEvent_t after) {
   constexpr int smem = decode_smem_bytes<D, kFp8, NST>();
-  auto kern = decode_kernel<D, kFp8, NST>;
+  auto kern = decode_kernel<D, kFp8, NST, RT>;
   LaunchInfo li;
   cudaError_t e = launch_info(kern, kDecodeWarps * 32, smem, &li);
   if (e != cudaSuccess) return e;
   const int sms = li.sms, per_sm = li.per_sm;
-  const int tpt = kRowsPerTile / p.group;
+  const int tpt = 8 * RT / p.group;
   const int64_t qtiles_max = (std::min(a.max_query_len, p.decode_max_query) + tpt - 1) / tpt;
   const int64_t upper = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads * qtiles_max * ws.pmax;
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(upper, int64_t(sms) * per_sm));
@@ -712,6 +743,14 @@ cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const CUtens
   p.score_log2 = a.scale * log2e * (fp8 ? a.cache.k_scale : 1.f);
   p.v_out_scale = fp8 ? a.cache.v_scale : 1.f;
 
+  // 16-row tiles when a tile of 8 rows cannot hold the group, or when the decode-path query
+  // runs (multi-token verify, short chunks) fill more than 8 rows; a mixed batch whose chunks
+  // go to the prefill path keeps 8-row tiles for its single-token decodes.
+  const int dec_q = std::min(a.max_query_len, p.decode_max_query);
+  const bool mixed = prefill && a.max_query_len > kDecodeMaxQuery;
+  const bool rt2 = p.group > 8 || (!mixed && static_cast<int64_t>(dec_q) * p.group > 8);
+  p.rows_per_tile = rt2 ? 16 : 8;
+
   plan_kernel<<<1, 1024, 0, a.stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -719,9 +758,14 @@ cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const CUtens
     e = launch_prefill(a, p.pf_item_start, p.hdr, *qmap, kmap, vmap);
     if (e != cudaSuccess) return e;
   }
-  if (fp8) return run_decode<128, true, 4>(a, ws, p, kmap, vmap, before, after);
-  if (a.head_dim == 128) return run_decode<128, false, 3>(a, ws, p, kmap, vmap, before, after);
-  return run_decode<64, false, 4>(a, ws, p, kmap, vmap, before, after);
+  if (fp8)
+    return rt2 ? run_decode<128, true, 4, 2>(a, ws, p, kmap, vmap, before, after)
+               : run_decode<128, true, 4, 1>(a, ws, p, kmap, vmap, before, after);
+  if (a.head_dim == 128)
+    return rt2 ? run_decode<128, false, 3, 2>(a, ws, p, kmap, vmap, before, after)
+               : run_decode<128, false, 3, 1>(a, ws, p, kmap, vmap, before, after);
+  return rt2 ? run_decode<64, false, 4, 2>(a, ws, p, kmap, vmap, before, after)
+             : run_decode<64, false, 4, 1>(a, ws, p, kmap, vmap, before, after);
 }
 
 }  // namespace pa

@@ -24,7 +24,8 @@ struct WsHeader {
 
 constexpr int kBlockSize = 16;            // tokens per physical block
 constexpr int kDecodeWarps = 4;           // warps per decode CTA
-constexpr int kRowsPerTile = 8;           // (query token x GQA head) rows per decode item
+constexpr int kRowsPerTile = 8;           // (query token x GQA head) rows of a small decode tile
+constexpr int kDecodeMaxGroup = 16;      // q heads per kv head: up to 16 rows of one item
 constexpr int kDecodeMaxQuery = 16;       // sequences with n_s above this use the prefill path
 constexpr float kLazyRescaleLog2 = 8.f;  // softmax base moves only past 2^8 growth
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per bounded wait

@@ -127,7 +127,7 @@ def _attn(lib, **kw):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(hq=6, hkv=4), 1),                 # not a multiple
-    (dict(hq=64, hkv=4), 2),                # group of 16 not built
+    (dict(hq=128, hkv=4), 2),               # group of 32 not built
     (dict(dim=128), 1),                     # disagrees with the descriptor
     (dict(odt=1), 2),                       # fp8 output not built
     (dict(scale=float("nan")), 1),

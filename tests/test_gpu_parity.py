@@ -64,6 +64,7 @@ EDGE_CTX = [1, 15, 16, 17, 32, 33, 100, 511, 512, 513, 2000]
     (4, 4, 128, "bf16"), (8, 4, 128, "bf16"), (16, 4, 128, "bf16"), (32, 4, 128, "bf16"),
     (4, 4, 64, "bf16"), (16, 2, 64, "bf16"),
     (8, 8, 128, "fp8_e4m3"), (16, 4, 128, "fp8_e4m3"), (32, 4, 128, "fp8_e4m3"),
+    (64, 4, 128, "bf16"), (32, 2, 64, "bf16"), (64, 4, 128, "fp8_e4m3"),     # groups of 16
 ])
 def test_decode_edge_lengths(hq, hkv, d, dtype):
     w = make_workload(EDGE_CTX, [1] * len(EDGE_CTX), num_q_heads=hq, num_kv_heads=hkv,
@@ -81,6 +82,22 @@ def test_decode_edge_lengths(hq, hkv, d, dtype):
 def test_multi_query_causal(qlens, ctx, dtype):
     w = make_workload(ctx, qlens, num_q_heads=16, num_kv_heads=4, head_dim=128,
                       cache_dtype=dtype, seed=sum(ctx), pool_fill="nan")
+    _check_small(w)
+
+
+@pytest.mark.parametrize("hq,hkv,qlens,ctx", [
+    (8, 8, [9, 16, 3, 1], [9, 700, 40, 2000]),        # MHA: up to 16 tokens in one 16-row tile
+    (8, 2, [5, 5, 1, 3], [517, 64, 1500, 3]),         # 4 x 4 rows, tail tile of one token
+    (64, 4, [1, 2, 5, 16], [33, 1000, 5, 300]),       # group of 16: one token per tile
+    (32, 2, [100, 1, 40], [2000, 77, 40]),            # group of 16 with long chunks
+    (24, 8, [7, 2, 11], [7, 260, 900]),               # group of 3: 5 tokens (15 rows) a tile
+])
+@pytest.mark.parametrize("dtype", ["bf16", "fp8_e4m3"])
+def test_multi_query_row_tiles(hq, hkv, qlens, ctx, dtype):
+    """Multi-query runs whose (token x head) rows fill 16-row decode tiles, groups of up to 16
+    q heads per kv head, and groups that do not divide the tile."""
+    w = make_workload(ctx, qlens, num_q_heads=hq, num_kv_heads=hkv, head_dim=128,
+                      cache_dtype=dtype, seed=hq + sum(ctx), pool_fill="nan")
     _check_small(w)
 
 
@@ -292,3 +309,26 @@ def test_config5_full_size_sampled():
 def test_speculative_verify_workload_sampled():
     """Multi-query verify step (1 accepted + 4 draft tokens per sequence, causal among them)."""
     _sampled(6, 6)
+
+
+def test_step_replays_from_a_cuda_graph():
+    """The library's calls are stream-ordered with no host synchronisation: a whole step
+    (append + attention) captured in a CUDA graph and replayed gives the eager result."""
+    h = _h()
+    w = make_workload([300, 1000, 2500, 40], [1, 1, 37, 1], num_q_heads=16, num_kv_heads=4,
+                      head_dim=128, seed=123)
+    d, out_eager = h.run_gpu(w)
+    out_eager = out_eager.clone()
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        d.step()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph, stream=cap):
+        d.step()
+    d.out.zero_()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(d.out, out_eager)
