@@ -170,7 +170,7 @@ template <int D, bool kFp8, int NST>
 constexpr int decode_smem_bytes() {
   using C = DecodeCfg<D, kFp8>;
   return 1024 /*alignment slack*/ + kDecodeWarps * NST * C::kStageBytes +
-         kDecodeWarps * NST * 8 /*mbarriers*/ + 64 /*item slot*/;
+         kDecodeWarps * NST * 8 /*mbarriers*/ + 2 * 64 /*item slots*/;
 }
 
 struct ItemInfo {
@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
   // RT row tiles of 8 rows: rows quad and quad + 8 of the m16 MMA (RT = 2 uses both halves)
   using C = DecodeCfg<D, kFp8>;
   constexpr int R = 8 * RT;
-  static_assert(C::kStageBytes * NST >= 16 * D * 4 + 2 * 16 * 4,
+  static_assert(sizeof(ItemInfo) <= 64 && C::kStageBytes * NST >= 16 * D * 4 + 2 * 16 * 4,
                 "merge scratch must fit in a warp's stage buffers");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -211,45 +211,50 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
   uint32_t it = 0;          // blocks this warp has consumed so far (stage / phase tracking)
   bool timed_out = false;
 
-  while (true) {
-    if (threadIdx.x == 0) {
-      ItemInfo info;
-      const int item = static_cast<int>(atomicAdd(&p.hdr->decode_counter, 1u));
-      info.valid = item < total_items;
-      if (info.valid) {
-        int lo = 0, hi = p.num_seqs;  // largest s with item_start[s] <= item
-        while (hi - lo > 1) {
-          const int mid = (lo + hi) >> 1;
-          if (p.item_start[mid] <= item) lo = mid; else hi = mid;
-        }
-        const int s = lo;
-        const int t0 = p.qsl[s];
-        const int n = p.qsl[s + 1] - t0;
-        const int L = p.context_lens[s];
-        const int tpt = R / p.group;
-        const int qtiles = ceil_div(n, tpt);
-        const int nblk = ceil_div(L, kBlockSize);
-        const int nparts = ceil_div(nblk, p.pblk);
-        int local = item - p.item_start[s];
-        const int part = local % nparts;
-        local /= nparts;
-        const int qt = local % qtiles;
-        const int h = local / qtiles;
-        const int tok_begin = qt * tpt;
-        const int tok_end = min(n, tok_begin + tpt);
-        const int pos_max = L - n + tok_end - 1;           // last position in the tile
-        const int blk_tile = pos_max / kBlockSize + 1;     // blocks the tile can see
-        info.s = s; info.h = h; info.qt = qt; info.part = part; info.t0 = t0 + tok_begin;
-        info.n = tok_end - tok_begin; info.L = L; info.nparts = nparts;
-        info.blk_begin = min(part * p.pblk, blk_tile);
-        info.blk_end = min((part + 1) * p.pblk, blk_tile);
-        info.pos_base = L - n + tok_begin;                 // position of the tile's first token
-        info.rows = info.n * p.group;
+  // Thread 0 claims and decodes the CTA's next item while the current one streams, so the
+  // atomic and the search over item_start stay off the critical path.
+  auto fetch_item = [&](ItemInfo* dst) {
+    ItemInfo info;
+    const int item = static_cast<int>(atomicAdd(&p.hdr->decode_counter, 1u));
+    info.valid = item < total_items;
+    if (info.valid) {
+      int lo = 0, hi = p.num_seqs;  // largest s with item_start[s] <= item
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (p.item_start[mid] <= item) lo = mid; else hi = mid;
       }
-      *s_item = info;
+      const int s = lo;
+      const int t0 = p.qsl[s];
+      const int n = p.qsl[s + 1] - t0;
+      const int L = p.context_lens[s];
+      const int tpt = R / p.group;
+      const int qtiles = ceil_div(n, tpt);
+      const int nblk = ceil_div(L, kBlockSize);
+      const int nparts = ceil_div(nblk, p.pblk);
+      int local = item - p.item_start[s];
+      const int part = local % nparts;
+      local /= nparts;
+      const int qt = local % qtiles;
+      const int h = local / qtiles;
+      const int tok_begin = qt * tpt;
+      const int tok_end = min(n, tok_begin + tpt);
+      const int pos_max = L - n + tok_end - 1;           // last position in the tile
+      const int blk_tile = pos_max / kBlockSize + 1;     // blocks the tile can see
+      info.s = s; info.h = h; info.qt = qt; info.part = part; info.t0 = t0 + tok_begin;
+      info.n = tok_end - tok_begin; info.L = L; info.nparts = nparts;
+      info.blk_begin = min(part * p.pblk, blk_tile);
+      info.blk_end = min((part + 1) * p.pblk, blk_tile);
+      info.pos_base = L - n + tok_begin;                 // position of the tile's first token
+      info.rows = info.n * p.group;
     }
+    *dst = info;
+  };
+  if (threadIdx.x == 0) fetch_item(&s_item[0]);
+  int cur = 0;
+
+  while (true) {
     const bool any_timeout = __syncthreads_or(timed_out) != 0;
-    const ItemInfo I = *s_item;
+    const ItemInfo I = s_item[cur];
     if (!I.valid || any_timeout) break;
     const uint32_t it0 = it;  // blocks consumed before this item
 
@@ -301,6 +306,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 
     const int npre = min(NST, nb_w);
     for (int k = 0; k < npre; ++k) issue(k);
+    if (threadIdx.x == 0) fetch_item(&s_item[cur ^ 1]);  // read after the next loop-top barrier
 
     // ---- q fragments (A operand of S = Q K^T): a0/a2 row quad, a1/a3 row quad + 8 -------
     uint32_t qa[C::kKSteps][4];
@@ -604,6 +610,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     }
     __syncthreads();
     fence_proxy_async_smem();  // generic accesses to the stage buffers before the next TMA
+    cur ^= 1;
   }
 }
 
