@@ -9,9 +9,10 @@
 //  * One work item = (sequence, kv head, tile of 128 rows), a row being (query token, q head of
 //    the GQA group), so the tile's queries share every K/V tile they read.  Items are taken
 //    longest-first from an atomic counter by persistent CTAs (one per SM).
-//  * Warp 0 issues TMA copies: the q tile once (a 3-D box of tokens x heads x 64 columns, two
-//    boxes), then for every 128 keys the 8 (block, kv head) K tiles and V tiles of the block
-//    table, into three-stage K and V rings (128-byte swizzle, completion on mbarriers).
+//  * Warp 0 issues TMA copies of the q tile once (a 3-D box of tokens x heads x 64 columns, two
+//    boxes), then for every 128 keys the 8 (block, kv head) K tiles of the block table; warp 6
+//    does the same for the V tiles.  Eight lanes of each issue one block's boxes apiece, into
+//    three-stage K and V rings (128-byte swizzle, completion on mbarriers).
 //  * Warp 1 issues tcgen05.mma from one thread: S = Q K^T into one of two TMEM buffers
 //    (128 x 128 fp32), and O += P V into a third, with P read from TMEM and V from shared
 //    memory (MN-major).  The softmax threads write P back over their S buffer as bf16 hi and lo
@@ -42,7 +43,8 @@ constexpr int kTile = 32768;  // 128 x 128 bf16
 constexpr int kQ = 0, kK = kTile, kV = kK + kStages * kTile;
 constexpr int kCtl = kV + kStages * kTile;  // control block (barriers, item, flags)
 constexpr int kSmem = 1024 + kCtl + 256;
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
+constexpr int kVWarp = 6;     // V producer (warp 0 loads q and K)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = kSBufs * 128;
 constexpr float kRescaleLog2 = 8.f;
@@ -170,9 +172,11 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     const PfItem I = ctl->item;
     if (!I.valid || ctl->abort_flag) break;
 
-    if (warp == 0) {
-      // ------------------------------------------------------------- producer (TMA) -----
-      if (lane == 0) {
+    if (warp == 0 || warp == pf::kVWarp) {
+      // ------------------------------------------------------- producers (TMA): warp 0 q and K,
+      // warp 6 V.  Two issuing warps double the rate at which tile copies enter the TMA unit.
+      const bool k_side = warp == 0;
+      if (k_side && lane == 0) {
         mbar_arrive_expect_tx(&ctl->q_full, pf::kTile);
         tma_load_3d(smem + pf::kQ, &qmap, 0, I.h * G, I.t0, &ctl->q_full);
         tma_load_3d(smem + pf::kQ + pf::kHalf, &qmap, 64, I.h * G, I.t0, &ctl->q_full);
@@ -248,22 +252,11 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         }
         return true;
       };
-      // K runs one slice ahead of V: S needs K three tiles before P V needs V
-      int ph_cur;
-      uint32_t ok_cur, bad_cur;
-      slice(0, ph_cur, ok_cur, bad_cur);
-      bool pok = load_k(0, ph_cur, ok_cur);
-      for (int j = 0; pok && j < I.nkv; ++j) {
-        int ph_nxt = -1;
-        uint32_t ok_nxt = 0, bad_nxt = 0;
-        if (j + 1 < I.nkv) {
-          slice(j + 1, ph_nxt, ok_nxt, bad_nxt);
-          pok = load_k(j + 1, ph_nxt, ok_nxt);
-        }
-        if (pok) pok = load_v(j, ph_cur, ok_cur, bad_cur);
-        ph_cur = ph_nxt;
-        ok_cur = ok_nxt;
-        bad_cur = bad_nxt;
+      for (int j = 0; j < I.nkv; ++j) {
+        int ph;
+        uint32_t okm, badm;
+        slice(j, ph, okm, badm);
+        if (!(k_side ? load_k(j, ph, okm) : load_v(j, ph, okm, badm))) break;
       }
     } else if (warp == 1) {
       // ------------------------------------------------------------- MMA issuer ---------
