@@ -44,6 +44,7 @@ sys.path.insert(0, ROOT)
 METRIC = "paged-attn step: achieved HBM GB/s (% of peak), attended tokens/s"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def parse_args(argv=None):
@@ -224,6 +225,14 @@ class DeviceWorkload:
         self.step()
         self.out_host.copy_(self.out, non_blocking=True)
 
+    def has_prefill(self) -> bool:
+        """Whether the step launches the tensor-core prefill-tile kernel (chunks of more than
+        16 queries over a bf16 pool with head_dim 128 and a group that divides 128)."""
+        w = self.w
+        g = w.num_q_heads // w.num_kv_heads
+        return (w.max_query_len > 16 and w.cache_dtype == "bf16" and w.head_dim == 128
+                and 128 % g == 0)
+
     def launches_per_step(self) -> int:
         """Our kernels one step launches: the append, the plan, the split-KV attention, the LSE
         merge when the workspace carries split partials, and the tensor-core prefill kernel
@@ -233,10 +242,17 @@ class DeviceWorkload:
                                                 w.num_kv_heads, w.head_dim, w.max_context_len,
                                                 w.max_query_len)
         no_partials = 256 + 2 * (((4 * (w.num_seqs + 1) + 255) // 256) * 256)
-        g = w.num_q_heads // w.num_kv_heads
-        prefill = (w.max_query_len > 16 and w.cache_dtype == "bf16" and w.head_dim == 128
-                   and 128 % g == 0)
-        return 3 + (1 if size > no_partials else 0) + (1 if prefill else 0)
+        return 3 + (1 if size > no_partials else 0) + (1 if self.has_prefill() else 0)
+
+
+def prefill_flops(w) -> int:
+    """Algorithmic flops of the prefill-tile kernel: every query of a chunk longer than 16
+    tokens against the keys it attends, QK^T and PV at 2 flops per multiply-add each."""
+    total = 0
+    for L, n in zip(w.context_lens.tolist(), w.query_lens.tolist()):
+        if n > 16:
+            total += n * (L - n) + n * (n + 1) // 2
+    return 4 * w.head_dim * w.num_q_heads * total
 
 
 def decode_src_sha() -> str:
@@ -371,6 +387,10 @@ def run_ours(args):
     dw = DeviceWorkload(w, device)
     algo_attn = w.algorithmic_bytes()
     algo_step = algo_attn + w.append_bytes()
+    # the split-KV kernel's own bytes: chunks on the tensor-core prefill path are not its work
+    decode_seqs = [s for s in range(w.num_seqs)
+                   if not (dw.has_prefill() and int(w.query_lens[s]) > 16)]
+    algo_decode = w.algorithmic_bytes(seqs=decode_seqs)
     stream = torch.cuda.current_stream(device)
 
     # warm-up (also checks the device error word once)
@@ -395,7 +415,9 @@ def run_ours(args):
     K = args.steps
     kb = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ka = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    for e in kb + ka:       # create the events before handing their handles to the library
+    pfb = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    pfa = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for e in kb + ka + pfb + pfa:   # create the events before handing them to the library
         e.record(stream)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -409,10 +431,12 @@ def run_ours(args):
     start.record(stream)
     for i in range(K):
         pa.set_kernel_timing_events(kb[i], ka[i])
+        pa.set_prefill_timing_events(pfb[i], pfa[i])
         dw.step()
     stop.record(stream)
     torch.cuda.synchronize(device)
     pa.set_kernel_timing_events(None, None)
+    pa.set_prefill_timing_events(None, None)
     # (2) graph replays: the timed steps of `value`
     barrier(dist, device)
     torch.cuda.synchronize(device)
@@ -425,6 +449,8 @@ def run_ours(args):
     clk = clocks.stop()
     assert pa.check_error(dw.ws) == 0
     kern_ms = statistics.mean(kb[i].elapsed_time(ka[i]) for i in range(K))
+    pf_flops = prefill_flops(w) if dw.has_prefill() else 0
+    pf_ms = statistics.mean(pfb[i].elapsed_time(pfa[i]) for i in range(K)) if pf_flops else None
     step_ms = max_over_ranks(g0.elapsed_time(g1) / K, dist, device)
     eager_ms = max_over_ranks(start.elapsed_time(stop) / K, dist, device)
 
@@ -444,7 +470,7 @@ def run_ours(args):
 
     peak, peak_kind, _ = load_peaks()
     value = world * algo_step / (step_ms * 1e-3) / 1e9
-    achieved = algo_attn / (kern_ms * 1e-3) / 1e9
+    achieved = algo_decode / (kern_ms * 1e-3) / 1e9
     result = None
     if rank == 0:
         cpu = None
@@ -478,11 +504,24 @@ def run_ours(args):
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
                          "traffic": traffic_from_profiles(args.config),
-                         "algorithmic_bytes_per_launch": algo_attn,
+                         "algorithmic_bytes_per_launch": algo_decode,
                          "kernel_ms": kern_ms},
             "cpu_baseline": cpu,
             "clocks": clk,
         }
+        if pf_flops:
+            peaks = load_peaks()[2]
+            pf_peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+            pf_tf = pf_flops / (pf_ms * 1e-3) / 1e12
+            result["prefill"] = {
+                "bound": "tensor", "kernel": "prefill_kernel (tcgen05 causal tiles)",
+                "achieved": pf_tf, "peak": pf_peak, "unit": "TFLOP/s", "frac": pf_tf / pf_peak,
+                "peak_source": ("measured" if "bf16_tflops" in peaks else "fallback")
+                               + " bf16_tflops (burst)",
+                "flops_per_launch": pf_flops, "kernel_ms": pf_ms,
+                "flops": "algorithmic: 4 * head_dim * q heads * attended keys of the chunk "
+                         "queries (QK^T and PV); masked tile parts and the second (lo) half "
+                         "of P's bf16 split are extra MMA work not counted"}
         print(json.dumps(result), flush=True)
     if dist is not None:
         dist.destroy_process_group()

@@ -201,6 +201,11 @@ const char* pa_version(void);
  * immediately after, its main attention kernel, on the call's stream.  Pass NULLs to stop. */
 void pa_set_kernel_timing_events(void* before, void* after);
 
+/* Benchmark hook, like pa_set_kernel_timing_events, for the tensor-core prefill-tile kernel
+ * (launched only by steps that hold chunks of more than 16 queries over a bf16 pool with
+ * head_dim 128).  Pass NULLs to stop. */
+void pa_set_prefill_timing_events(void* before, void* after);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,7 +24,8 @@ from ._lib import (PA_BF16, PA_FP8_E4M3, PA_FP32, PA_WORKSPACE_HEADER_BYTES,  # 
                    PagedAttnError)
 
 __all__ = ["cache_append", "attention", "attention_workspace_size", "new_workspace",
-           "check_error", "library", "version", "PagedAttnError", "set_kernel_timing_events"]
+           "check_error", "library", "version", "PagedAttnError", "set_kernel_timing_events",
+           "set_prefill_timing_events"]
 
 
 def library() -> ctypes.CDLL:
@@ -156,3 +157,12 @@ def set_kernel_timing_events(before: Optional[torch.cuda.Event],
     b = ctypes.c_void_p(before.cuda_event) if before is not None else ctypes.c_void_p(0)
     a = ctypes.c_void_p(after.cuda_event) if after is not None else ctypes.c_void_p(0)
     _lib.load().pa_set_kernel_timing_events(b, a)
+
+
+def set_prefill_timing_events(before: Optional[torch.cuda.Event],
+                              after: Optional[torch.cuda.Event]) -> None:
+    """Have later attention calls of this thread record `before`/`after` around their
+    tensor-core prefill-tile kernel, when they launch one (benchmark hook); None stops."""
+    b = ctypes.c_void_p(before.cuda_event) if before is not None else ctypes.c_void_p(0)
+    a = ctypes.c_void_p(after.cuda_event) if after is not None else ctypes.c_void_p(0)
+    _lib.load().pa_set_prefill_timing_events(b, a)

@@ -20,7 +20,8 @@ STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED",
 
 EXPORTED = ["pa_cache_append", "pa_attention_workspace_size", "pa_attention", "pa_check_error",
             "pa_workspace_init", "pa_last_error_string", "pa_version",
-            "pa_set_kernel_timing_events", "pa_attention_noalloc", "pa_copy_blocks"]
+            "pa_set_kernel_timing_events", "pa_set_prefill_timing_events",
+            "pa_attention_noalloc", "pa_copy_blocks"]
 EXPORTED_BM = ["pa_bm_create", "pa_bm_destroy", "pa_bm_num_free", "pa_bm_append",
                "pa_bm_append_tokens", "pa_bm_fork", "pa_bm_free", "pa_bm_block_table",
                "pa_bm_num_tokens", "pa_bm_refcount", "pa_bm_cached_prefix"]
@@ -100,6 +101,8 @@ def load() -> ctypes.CDLL:
     L.pa_version.restype = ctypes.c_char_p
     L.pa_set_kernel_timing_events.argtypes = [vp, vp]
     L.pa_set_kernel_timing_events.restype = None
+    L.pa_set_prefill_timing_events.argtypes = [vp, vp]
+    L.pa_set_prefill_timing_events.restype = None
     _LIB = L
     return L
 

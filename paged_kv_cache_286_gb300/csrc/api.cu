@@ -19,6 +19,8 @@ namespace {
 thread_local std::string g_last_error;
 thread_local cudaEvent_t g_before = nullptr;
 thread_local cudaEvent_t g_after = nullptr;
+thread_local cudaEvent_t g_pf_before = nullptr;
+thread_local cudaEvent_t g_pf_after = nullptr;
 
 pa_status fail(pa_status st, const char* fmt, ...) {
   char buf[512];
@@ -205,6 +207,11 @@ void pa_set_kernel_timing_events(void* before, void* after) {
   g_after = static_cast<cudaEvent_t>(after);
 }
 
+void pa_set_prefill_timing_events(void* before, void* after) {
+  g_pf_before = static_cast<cudaEvent_t>(before);
+  g_pf_after = static_cast<cudaEvent_t>(after);
+}
+
 pa_status pa_workspace_init(void* workspace, cudaStream_t stream) {
   g_last_error.clear();
   if (!workspace) return fail(PA_ERR_INVALID_ARG, "workspace is NULL");
@@ -337,6 +344,8 @@ pa_status pa_attention(const void* q, int32_t num_q_tokens, const void* k_cache,
                  context_lens, query_start_loc, num_seqs, max_context_len, max_query_len,
                  num_q_heads, num_kv_heads, head_dim, scale, out, out_dtype, workspace,
                  workspace_bytes, stream};
+  a.pf_before = g_pf_before;
+  a.pf_after = g_pf_after;
   cudaError_t e =
       pa::launch_attention(a, ws, kmap, vmap, use_prefill ? &qmap : nullptr, g_before, g_after);
   if (e != cudaSuccess) return cuda_fail(e, "pa_attention launch");

@@ -49,6 +49,8 @@ struct AttnArgs {
   void* workspace;
   size_t workspace_bytes;
   cudaStream_t stream;
+  cudaEvent_t pf_before = nullptr;  // benchmark hook: recorded around the prefill kernel
+  cudaEvent_t pf_after = nullptr;
 };
 
 // Workspace carve-up; a pure function of the step's shape (see workspace_layout).

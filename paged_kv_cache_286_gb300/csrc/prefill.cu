@@ -493,8 +493,10 @@ cudaError_t launch_prefill(const AttnArgs& a, const int32_t* item_start, WsHeade
       static_cast<int64_t>(a.num_kv_heads) *
       ((static_cast<int64_t>(a.num_q_tokens) * G + pf::kRows - 1) / pf::kRows + a.num_seqs);
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(upper, sms));
+  if (a.pf_before && a.pf_after) cudaEventRecord(a.pf_before, a.stream);
   prefill_kernel<<<static_cast<unsigned>(grid), pf::kThreads, pf::kSmem, a.stream>>>(qmap, kmap,
                                                                                      vmap, p);
+  if (a.pf_before && a.pf_after) cudaEventRecord(a.pf_after, a.stream);
   return cudaGetLastError();
 }
 

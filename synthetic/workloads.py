@@ -148,23 +148,27 @@ class Workload:
             total += n * L - n * (n - 1) // 2
         return total
 
-    def unique_blocks(self) -> int:
-        """Physical blocks referenced by the step (a shared block counts once)."""
+    def unique_blocks(self, seqs: Optional[Sequence[int]] = None) -> int:
+        """Physical blocks referenced by the step, or by the sequences `seqs` (a shared block
+        counts once)."""
         ids = set()
-        for s in range(self.num_seqs):
+        for s in (range(self.num_seqs) if seqs is None else seqs):
             nb = -(-int(self.context_lens[s]) // self.block_size)
             ids.update(self.block_tables[s, :nb].tolist())
         return len(ids)
 
-    def algorithmic_bytes(self, out_bytes_per_elem: int = 4) -> int:
+    def algorithmic_bytes(self, out_bytes_per_elem: int = 4,
+                          seqs: Optional[Sequence[int]] = None) -> int:
         """Bytes a perfect implementation moves for the attention: unique K/V blocks touched
-        (whole blocks, shared ones once), q read, out written, and the metadata read."""
-        kv = 2 * self.unique_blocks() * self.num_kv_heads * self.block_size * self.head_dim \
-            * self.cache_elem_bytes
-        T = self.num_tokens
+        (whole blocks, shared ones once), q read, out written, and the metadata read; over all
+        sequences or only over `seqs`."""
+        idx = list(range(self.num_seqs)) if seqs is None else list(seqs)
+        kv = 2 * self.unique_blocks(idx) * self.num_kv_heads * self.block_size * \
+            self.head_dim * self.cache_elem_bytes
+        T = int(sum(int(self.query_lens[s]) for s in idx))
         qo = T * self.num_q_heads * self.head_dim * (2 + out_bytes_per_elem)
-        meta = 4 * (self.num_seqs * 2 + 1) + 4 * sum(
-            -(-int(L) // self.block_size) for L in self.context_lens.tolist())
+        meta = 4 * (len(idx) * 2 + 1) + 4 * sum(
+            -(-int(self.context_lens[s]) // self.block_size) for s in idx)
         return int(kv + qo + meta)
 
     def append_bytes(self) -> int:
