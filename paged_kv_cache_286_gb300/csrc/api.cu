@@ -334,7 +334,7 @@ pa_status pa_attention(const void* q, int32_t num_q_tokens, const void* k_cache,
 
   CUtensorMap qmap;
   const bool use_prefill = pa::prefill_path_enabled(*cache, num_q_heads, num_kv_heads) &&
-                           max_query_len > pa::kDecodeMaxQuery;
+                           pa::routes_to_prefill(max_query_len, num_q_heads / num_kv_heads);
   if (use_prefill &&
       (st = encode_q_map(&qmap, q, num_q_tokens, num_q_heads, head_dim,
                          num_q_heads / num_kv_heads)) != PA_OK)

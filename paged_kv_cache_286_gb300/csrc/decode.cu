@@ -9,8 +9,10 @@
 //  * Work item = (sequence, kv head, tile of 8 or 16 rows, KV partition of `pblk` blocks).  A row
 //    is a (query token, q head of the GQA group) pair, so one item loads each K/V block once for
 //    the whole group and for as many of the sequence's query tokens as the tile holds.  16-row
-//    tiles (both halves of the MMA's M) serve groups above 8 and multi-token runs (speculative
-//    verify, short chunks); single-token decode keeps 8-row tiles, the cheaper instance.  A plan kernel turns context lengths into per-sequence item counts; the
+//    tiles (both halves of the MMA's M) serve groups above 8 and multi-token runs of up to 16
+//    rows; single-token decode keeps 8-row tiles, the cheaper instance.  Runs with more rows
+//    (long chunks, speculative verify with GQA) go to the tensor-core prefill tiles when those
+//    are built for the pool, and otherwise take several tiles here.  A plan kernel turns context lengths into per-sequence item counts; the
 //    attention kernel is persistent and takes items from an atomic counter.
 //  * Each of the CTA's 4 warps owns every 4th block of the partition and streams it through its
 //    own ring of shared-memory stages: one lane issues 2-D TMA tile copies of the (block, head)
@@ -54,7 +56,8 @@ struct DecodeParams {
   int32_t max_query_len;
   int32_t pblk;
   int32_t pmax;
-  int32_t decode_max_query;
+  int32_t decode_max_query;  // longer query runs go to the prefill-tile path
+  int32_t decode_max_rows;   // so do runs of more (token x head) rows than one decode tile
   int32_t rows_per_tile;   // 8 * RT of the decode kernel instance
   int32_t out_bf16;
   float score_log2;        // scale * log2(e) (* k_scale for E4M3)
@@ -75,7 +78,7 @@ __device__ __forceinline__ int decode_items_of(const DecodeParams& p, int n, int
     *bad = true;
     return 0;
   }
-  if (n > p.decode_max_query) return 0;
+  if (n > p.decode_max_query || n * p.group > p.decode_max_rows) return 0;
   const int tpt = p.rows_per_tile / p.group;  // query tokens per tile
   const int qtiles = ceil_div(n, tpt);
   const int nparts = ceil_div(ceil_div(L, kBlockSize), p.pblk);
@@ -85,7 +88,7 @@ __device__ __forceinline__ int decode_items_of(const DecodeParams& p, int n, int
 // Prefill-path items of one sequence: one per (kv head, 128-row tile of tokens x heads).
 __device__ __forceinline__ int prefill_items_of(const DecodeParams& p, int n, int L) {
   bool bad;
-  if (decode_items_of(p, n, L, &bad) != 0 || bad || n <= p.decode_max_query) return 0;
+  if (decode_items_of(p, n, L, &bad) != 0 || bad || n <= 0) return 0;
   const int tpt = 128 / p.group;
   return p.num_kv_heads * ceil_div(n, tpt);
 }
@@ -744,6 +747,7 @@ cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const CUtens
   const bool prefill = qmap != nullptr && prefill_path_enabled(a.cache, a.num_q_heads,
                                                                a.num_kv_heads);
   p.decode_max_query = prefill ? kDecodeMaxQuery : INT32_MAX;
+  p.decode_max_rows = prefill ? kDecodeMaxRows : INT32_MAX;
   p.out_bf16 = a.out_dtype == PA_BF16;
   const float log2e = 1.4426950408889634f;
   const bool fp8 = a.cache.cache_dtype == PA_FP8_E4M3;
@@ -754,7 +758,7 @@ cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const CUtens
   // runs (multi-token verify, short chunks) fill more than 8 rows; a mixed batch whose chunks
   // go to the prefill path keeps 8-row tiles for its single-token decodes.
   const int dec_q = std::min(a.max_query_len, p.decode_max_query);
-  const bool mixed = prefill && a.max_query_len > kDecodeMaxQuery;
+  const bool mixed = prefill && routes_to_prefill(a.max_query_len, p.group);
   const bool rt2 = p.group > 8 || (!mixed && static_cast<int64_t>(dec_q) * p.group > 8);
   p.rows_per_tile = rt2 ? 16 : 8;
 

@@ -26,7 +26,15 @@ constexpr int kBlockSize = 16;            // tokens per physical block
 constexpr int kDecodeWarps = 4;           // warps per decode CTA
 constexpr int kRowsPerTile = 8;           // (query token x GQA head) rows of a small decode tile
 constexpr int kDecodeMaxGroup = 16;      // q heads per kv head: up to 16 rows of one item
-constexpr int kDecodeMaxQuery = 16;       // sequences with n_s above this use the prefill path
+constexpr int kDecodeMaxQuery = 16;       // sequences with n_s above this use the prefill path,
+constexpr int kDecodeMaxRows = 16;        // and so do those with more n_s x G rows than this
+
+// Whether a query run of n tokens with G heads per kv head is served by the prefill-tile
+// kernel (when that kernel is built for the pool): more rows than one 16-row decode tile holds
+// share each K/V slice better in 128-row tensor-core tiles.
+__host__ __device__ constexpr bool routes_to_prefill(int n, int G) {
+  return n > kDecodeMaxQuery || n * G > kDecodeMaxRows;
+}
 constexpr float kLazyRescaleLog2 = 8.f;  // softmax base moves only past 2^8 growth
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per bounded wait
 

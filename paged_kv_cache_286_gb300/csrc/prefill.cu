@@ -4,6 +4,9 @@
 // sections "Chunked Prefill", "Prefill Versus Decode", "Attention Over Scattered Blocks"): a
 // prompt chunk of n tokens whose sequence holds L keys after this step's append sits at
 // positions p_i = L - n + i; token i attends keys 0..p_i, fetched through the block table.
+// The same causal run serves the verify step of speculative decoding (section "Speculative
+// Decoding": the draft tokens are checked in one pass); every run of more than 16 tokens or
+// more than 16 (token x head) rows comes here.
 //
 // Design (GB300 / sm_103a; bf16 K/V, head_dim 128):
 //  * One work item = (sequence, kv head, tile of 128 rows), a row being (query token, q head of
@@ -338,6 +341,17 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         if (!(ok = wait(&ctl->s_full[b], (g / pf::kSBufs) & 1u))) break;
         tc_fence_after();
         const int kmax = row_ok ? row_pos - j * pf::kKeys : -1;  // keys 0..kmax are visible
+        if (!__any_sync(0xffffffffu, row_ok)) {  // a quarter of rows past the run: P = 0
+          uint32_t z[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) z[e] = 0u;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) tmem_st16(tl + b * 128u + c * 16, z);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&ctl->p_full[b]);
+          continue;
+        }
         uint32_t sv[128];
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -349,7 +363,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         float mx[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx[i] = -CUDART_INF_F;
-        if (kmax >= pf::kKeys - 1) {
+        if (__all_sync(0xffffffffu, kmax >= pf::kKeys - 1)) {  // warp-uniform branch
 #pragma unroll
           for (int i = 0; i < 128; ++i) {
             x[i] = __uint_as_float(sv[i]) * p.score_log2;
