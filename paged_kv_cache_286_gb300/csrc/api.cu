@@ -190,6 +190,40 @@ cudaError_t launch_info_impl(const void* kern, int threads, int smem_bytes, Laun
   return cudaSuccess;
 }
 
+cudaError_t side_stream(SideStream* out) {
+  // per thread and device, so that concurrent callers on other threads never wait on each
+  // other's prefill kernels
+  constexpr int kMaxDev = 64;
+  thread_local cudaStream_t streams[kMaxDev] = {};
+  thread_local cudaEvent_t forks[kMaxDev] = {};
+  thread_local cudaEvent_t joins[kMaxDev] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  if (!streams[dev]) {
+    int least = 0, greatest = 0;
+    if ((e = cudaDeviceGetStreamPriorityRange(&least, &greatest)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithPriority(&streams[dev], cudaStreamNonBlocking, greatest)) !=
+        cudaSuccess) {
+      streams[dev] = nullptr;
+      return e;
+    }
+  }
+  if (!forks[dev] && (e = cudaEventCreateWithFlags(&forks[dev], cudaEventDisableTiming)) !=
+                         cudaSuccess) {
+    forks[dev] = nullptr;
+    return e;
+  }
+  if (!joins[dev] && (e = cudaEventCreateWithFlags(&joins[dev], cudaEventDisableTiming)) !=
+                         cudaSuccess) {
+    joins[dev] = nullptr;
+    return e;
+  }
+  *out = SideStream{streams[dev], forks[dev], joins[dev]};
+  return cudaSuccess;
+}
+
 // Lets other translation units of the library report a host-side error through
 // pa_last_error_string.
 void set_last_error(const char* msg) { g_last_error = msg; }

@@ -765,18 +765,36 @@ cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const CUtens
   plan_kernel<<<1, 1024, 0, a.stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  // The prefill tiles (tensor pipe, key slices mostly from L2) and the split-KV decode (HBM)
+  // run side by side: the prefill kernel goes to a high-priority side stream forked from the
+  // caller's stream after the plan, so its CTAs are placed first and decode CTAs fill the SMs
+  // it leaves; the caller's stream joins it before returning.  Both paths only read what the
+  // plan wrote and write disjoint output rows.
+  SideStream side{};
   if (prefill) {
-    e = launch_prefill(a, p.pf_item_start, p.hdr, *qmap, kmap, vmap);
-    if (e != cudaSuccess) return e;
+    if ((e = side_stream(&side)) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(side.fork, a.stream)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(side.stream, side.fork, 0)) != cudaSuccess) return e;
+    AttnArgs b = a;
+    b.stream = side.stream;
+    if ((e = launch_prefill(b, p.pf_item_start, p.hdr, *qmap, kmap, vmap)) != cudaSuccess)
+      return e;
+    if ((e = cudaEventRecord(side.join, side.stream)) != cudaSuccess) return e;
   }
   if (fp8)
-    return rt2 ? run_decode<128, true, 4, 2>(a, ws, p, kmap, vmap, before, after)
-               : run_decode<128, true, 4, 1>(a, ws, p, kmap, vmap, before, after);
-  if (a.head_dim == 128)
-    return rt2 ? run_decode<128, false, 3, 2>(a, ws, p, kmap, vmap, before, after)
-               : run_decode<128, false, 3, 1>(a, ws, p, kmap, vmap, before, after);
-  return rt2 ? run_decode<64, false, 4, 2>(a, ws, p, kmap, vmap, before, after)
-             : run_decode<64, false, 4, 1>(a, ws, p, kmap, vmap, before, after);
+    e = rt2 ? run_decode<128, true, 4, 2>(a, ws, p, kmap, vmap, before, after)
+            : run_decode<128, true, 4, 1>(a, ws, p, kmap, vmap, before, after);
+  else if (a.head_dim == 128)
+    e = rt2 ? run_decode<128, false, 3, 2>(a, ws, p, kmap, vmap, before, after)
+            : run_decode<128, false, 3, 1>(a, ws, p, kmap, vmap, before, after);
+  else
+    e = rt2 ? run_decode<64, false, 4, 2>(a, ws, p, kmap, vmap, before, after)
+            : run_decode<64, false, 4, 1>(a, ws, p, kmap, vmap, before, after);
+  if (prefill) {
+    const cudaError_t j = cudaStreamWaitEvent(a.stream, side.join, 0);  // join even on error
+    if (e == cudaSuccess) e = j;
+  }
+  return e;
 }
 
 }  // namespace pa

@@ -90,6 +90,16 @@ cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const CUtens
                              cudaEvent_t before, cudaEvent_t after);
 
 struct WsHeader;
+// A high-priority stream of the current device for the prefill-tile kernel, and two events of
+// the calling thread to fork it from and join it to the caller's stream.  Created on first use
+// (per device; the events per thread and device) and kept for the life of the process.
+struct SideStream {
+  cudaStream_t stream;
+  cudaEvent_t fork;
+  cudaEvent_t join;
+};
+cudaError_t side_stream(SideStream* out);
+
 cudaError_t launch_prefill(const AttnArgs& a, const int32_t* item_start, WsHeader* hdr,
                            const CUtensorMap& qmap, const CUtensorMap& kmap,
                            const CUtensorMap& vmap);
