@@ -53,8 +53,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // 2-D view of a pool tensor: rows = num_blocks * num_kv_heads * block_size, cols = head_dim;
-// one box = 16 rows x 128 bytes with the 128-byte swizzle.
-pa_status encode_pool_map(CUtensorMap* map, const void* base, const pa_cache_desc& c) {
+// one box = 16 rows (times heads_per_box: the tiles of consecutive kv heads of a block are
+// consecutive rows) x 128 bytes with the 128-byte swizzle.
+pa_status encode_pool_map(CUtensorMap* map, const void* base, const pa_cache_desc& c,
+                          int heads_per_box = 1) {
   auto enc = tensor_map_encoder();
   if (!enc) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const bool fp8 = c.cache_dtype == PA_FP8_E4M3;
@@ -62,7 +64,8 @@ pa_status encode_pool_map(CUtensorMap* map, const void* base, const pa_cache_des
       static_cast<cuuint64_t>(c.num_blocks) * c.num_kv_heads * static_cast<cuuint64_t>(c.block_size);
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(c.head_dim), rows};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(c.head_dim) * (fp8 ? 1 : 2)};
-  const cuuint32_t box[2] = {fp8 ? 128u : 64u, static_cast<cuuint32_t>(c.block_size)};
+  const cuuint32_t box[2] = {fp8 ? 128u : 64u,
+                             static_cast<cuuint32_t>(c.block_size * heads_per_box)};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                    const_cast<void*>(base), dims, strides, box, estr,
@@ -363,8 +366,11 @@ pa_status pa_attention(const void* q, int32_t num_q_tokens, const void* k_cache,
     return fail(PA_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes,
                 ws.total);
   CUtensorMap kmap, vmap;
-  if ((st = encode_pool_map(&kmap, k_cache, *cache)) != PA_OK) return st;
-  if ((st = encode_pool_map(&vmap, v_cache, *cache)) != PA_OK) return st;
+  // boxes of one or two kv heads' rows (two only for single-token E4M3 decode, where no
+  // prefill tile reads these maps)
+  const int hpi = pa::decode_heads_per_item(*cache, num_q_heads, num_kv_heads, max_query_len);
+  if ((st = encode_pool_map(&kmap, k_cache, *cache, hpi)) != PA_OK) return st;
+  if ((st = encode_pool_map(&vmap, v_cache, *cache, hpi)) != PA_OK) return st;
 
   CUtensorMap qmap;
   const bool use_prefill = pa::prefill_path_enabled(*cache, num_q_heads, num_kv_heads) &&

@@ -59,6 +59,7 @@ struct DecodeParams {
   int32_t decode_max_query;  // longer query runs go to the prefill-tile path
   int32_t decode_max_rows;   // so do runs of more (token x head) rows than one decode tile
   int32_t rows_per_tile;   // 8 * RT of the decode kernel instance
+  int32_t heads_per_item;  // HPI of the decode kernel instance
   int32_t out_bf16;
   float score_log2;        // scale * log2(e) (* k_scale for E4M3)
   float v_out_scale;       // v_scale for E4M3, else 1
@@ -79,10 +80,10 @@ __device__ __forceinline__ int decode_items_of(const DecodeParams& p, int n, int
     return 0;
   }
   if (n > p.decode_max_query || n * p.group > p.decode_max_rows) return 0;
-  const int tpt = p.rows_per_tile / p.group;  // query tokens per tile
+  const int tpt = p.rows_per_tile / (p.group * p.heads_per_item);  // query tokens per tile
   const int qtiles = ceil_div(n, tpt);
   const int nparts = ceil_div(ceil_div(L, kBlockSize), p.pblk);
-  return p.num_kv_heads * qtiles * nparts;
+  return p.num_kv_heads / p.heads_per_item * qtiles * nparts;
 }
 
 // Prefill-path items of one sequence: one per (kv head, 128-row tile of tokens x heads).
@@ -158,20 +159,24 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
   }
 }
 
-template <int D, bool kFp8>
+template <int D, bool kFp8, int HPI = 1>
 struct DecodeCfg {
   static constexpr int kElem = kFp8 ? 1 : 2;
-  static constexpr int kTileBytes = kBlockSize * D * kElem;         // one (block, head) tile
+  static constexpr int kHeadBytes = kBlockSize * D * kElem;         // one (block, head) tile
+  static constexpr int kTileBytes = HPI * kHeadBytes;               // the item's heads of a block
   static constexpr int kBoxCols = kFp8 ? 128 : 64;                  // elements per 128-B row
   static constexpr int kBoxes = D / kBoxCols;                       // TMA boxes per tile
-  static constexpr int kBoxBytes = kBlockSize * 128;                // 16 rows x 128 B
-  static constexpr int kStageBytes = 2 * kTileBytes;                // K tile + V tile
+  static constexpr int kBoxBytes = HPI * kBlockSize * 128;          // 16 HPI rows x 128 B
+  static constexpr int kStageBytes = 2 * kTileBytes;                // K tiles + V tiles
   static constexpr int kKSteps = D / 16;
+  // consecutive kv heads of a block are consecutive rows of the pool, so one box of 16 HPI rows
+  // holds all of them only when a head's tile is one 128-byte column box (E4M3, D 128)
+  static_assert(HPI == 1 || kBoxes == 1, "several heads per item need one box per head tile");
 };
 
-template <int D, bool kFp8, int NST>
+template <int D, bool kFp8, int NST, int HPI>
 constexpr int decode_smem_bytes() {
-  using C = DecodeCfg<D, kFp8>;
+  using C = DecodeCfg<D, kFp8, HPI>;
   return 1024 /*alignment slack*/ + kDecodeWarps * NST * C::kStageBytes +
          kDecodeWarps * NST * 8 /*mbarriers*/ + 2 * 64 /*item slots*/;
 }
@@ -180,13 +185,16 @@ struct ItemInfo {
   int s, h, qt, part, t0, n, L, nparts, blk_begin, blk_end, pos_base, rows, valid;
 };
 
-template <int D, bool kFp8, int NST, int RT>
+template <int D, bool kFp8, int NST, int RT, int HPI>
 __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     decode_kernel(const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
-  // RT row tiles of 8 rows: rows quad and quad + 8 of the m16 MMA (RT = 2 uses both halves)
-  using C = DecodeCfg<D, kFp8>;
+  // RT row tiles of 8 rows: rows quad and quad + 8 of the m16 MMA (RT = 2 uses both halves).
+  // HPI kv heads per item (single-token decode only): row r is q head h0 * G + r, and the rows
+  // of head h0 + i take their scores from, and add P V into O from, head i's tiles alone.
+  using C = DecodeCfg<D, kFp8, HPI>;
   constexpr int R = 8 * RT;
+  static_assert(HPI == 1 || RT == 1, "several heads per item use one 8-row tile");
   static_assert(sizeof(ItemInfo) <= 64 && C::kStageBytes * NST >= 16 * D * 4 + 2 * 16 * 4,
                 "merge scratch must fit in a warp's stage buffers");
   extern __shared__ uint8_t smem_raw[];
@@ -230,7 +238,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
       const int t0 = p.qsl[s];
       const int n = p.qsl[s + 1] - t0;
       const int L = p.context_lens[s];
-      const int tpt = R / p.group;
+      const int tpt = R / (p.group * HPI);
       const int qtiles = ceil_div(n, tpt);
       const int nblk = ceil_div(L, kBlockSize);
       const int nparts = ceil_div(nblk, p.pblk);
@@ -238,7 +246,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
       const int part = local % nparts;
       local /= nparts;
       const int qt = local % qtiles;
-      const int h = local / qtiles;
+      const int h = (local / qtiles) * HPI;                // first kv head of the item
       const int tok_begin = qt * tpt;
       const int tok_end = min(n, tok_begin + tpt);
       const int pos_max = L - n + tok_end - 1;           // last position in the tile
@@ -248,7 +256,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
       info.blk_begin = min(part * p.pblk, blk_tile);
       info.blk_end = min((part + 1) * p.pblk, blk_tile);
       info.pos_base = L - n + tok_begin;                 // position of the tile's first token
-      info.rows = info.n * p.group;
+      info.rows = info.n * p.group * HPI;
     }
     *dst = info;
   };
@@ -268,9 +276,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     for (int r = 0; r < RT; ++r) {
       const int row = quad + 8 * r;
       row_ok[r] = row < I.rows;
-      row_tok[r] = row_ok[r] ? row / p.group : 0;
+      row_tok[r] = row_ok[r] ? row / (p.group * HPI) : 0;
       row_pos[r] = I.pos_base + row_tok[r];
     }
+    const int my_head = HPI > 1 ? quad / p.group : 0;  // head of the item this lane's row uses
     const int pos_last = I.pos_base + I.n - 1;
 
     // ---- table entries of this warp's blocks, one per lane -----------------------------
@@ -321,7 +330,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
       const int row = quad + 8 * r;
       const __nv_bfloat16* qrow =
           p.q + (static_cast<int64_t>(I.t0 + row_tok[r]) * p.num_q_heads + I.h * p.group +
-                 (row_ok[r] ? row % p.group : 0)) * D;
+                 (row_ok[r] ? row % (p.group * HPI) : 0)) * D;
       if constexpr (!kFp8) {
         row_scale[r] = p.score_log2;
 #pragma unroll
@@ -409,16 +418,26 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
             }
           } else {
 #pragma unroll
-            for (int kk = 0; kk < D / 64; ++kk) {
-              const int chunk = 4 * kk + (lane >> 3);  // 16-byte chunk = 16 d = one k-step
-              const uint32_t addr = kbase + krow * 128 + (((chunk & 7) ^ (krow & 7)) << 4);
-              uint32_t rr[4];
-              ldsm_x4(addr, rr[0], rr[1], rr[2], rr[3]);
+            for (int hi = 0; hi < HPI; ++hi) {
+              // head hi's scores; a lane keeps those of its own row's head
+              float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-              for (int m = 0; m < 4; ++m) {
-                uint32_t b0, b1;
-                e4m3x4_to_f16x2x2(rr[m], b0, b1);
-                mma_f16(sacc[nt], qa[4 * kk + m], b0, b1);
+              for (int kk = 0; kk < D / 64; ++kk) {
+                const int chunk = 4 * kk + (lane >> 3);  // 16-byte chunk = 16 d = one k-step
+                const uint32_t addr = kbase + hi * C::kHeadBytes + krow * 128 +
+                                      (((chunk & 7) ^ (krow & 7)) << 4);
+                uint32_t rr[4];
+                ldsm_x4(addr, rr[0], rr[1], rr[2], rr[3]);
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                  uint32_t b0, b1;
+                  e4m3x4_to_f16x2x2(rr[m], b0, b1);
+                  mma_f16(acc, qa[4 * kk + m], b0, b1);
+                }
+              }
+              if (hi == 0 || my_head == hi) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) sacc[nt][i] = acc[i];
               }
             }
           }
@@ -514,9 +533,19 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
         } else {
           const int vrow = ((lane >> 3) & 1) * 8 + (lane & 7);
 #pragma unroll
+          for (int hi = 0; hi < HPI; ++hi) {
+          // P^T columns of rows of other heads are zero for head hi's V
+          uint32_t pbh[RT][2];
+#pragma unroll
+          for (int r = 0; r < RT; ++r) {
+            pbh[r][0] = (HPI == 1 || my_head == hi) ? pb[r][0] : 0u;
+            pbh[r][1] = (HPI == 1 || my_head == hi) ? pb[r][1] : 0u;
+          }
+#pragma unroll
           for (int jj = 0; jj < D / 32; ++jj) {
             const int chunk = 2 * jj + (lane >> 4);
-            const uint32_t addr = vbase + vrow * 128 + (((chunk & 7) ^ (vrow & 7)) << 4);
+            const uint32_t addr = vbase + hi * C::kHeadBytes + vrow * 128 +
+                                  (((chunk & 7) ^ (vrow & 7)) << 4);
             uint32_t rr[4];  // (keys 0-7, chunk 2jj), (8-15, 2jj), (0-7, 2jj+1), (8-15, 2jj+1)
             ldsm_x4_t(addr, rr[0], rr[1], rr[2], rr[3]);
             if (nvalid < kBlockSize) {
@@ -532,8 +561,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
               e4m3x4_to_f16x2x2(prmt(rr[2 * h2], 0u, 0x3120u), a[0], a[1]);
               e4m3x4_to_f16x2x2(prmt(rr[2 * h2 + 1], 0u, 0x3120u), a[2], a[3]);
 #pragma unroll
-              for (int r = 0; r < RT; ++r) mma_f16(oacc[r][2 * jj + h2], a, pb[r][0], pb[r][1]);
+              for (int r = 0; r < RT; ++r) mma_f16(oacc[r][2 * jj + h2], a, pbh[r][0], pbh[r][1]);
             }
+          }
           }
         }
       }
@@ -597,8 +627,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
         }
       }
       const float val = Lsum > 0.f ? O / Lsum * p.v_out_scale : 0.f;
-      const int t = I.t0 + r / p.group;
-      const int hq = I.h * p.group + r % p.group;
+      const int t = I.t0 + r / (p.group * HPI);
+      const int hq = I.h * p.group + r % (p.group * HPI);
       const int64_t orow = static_cast<int64_t>(t) * p.num_q_heads + hq;
       if (I.nparts == 1) {
         if (p.out_bf16)
@@ -680,19 +710,20 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p, int32_
   }
 }
 
-template <int D, bool kFp8, int NST, int RT>
+template <int D, bool kFp8, int NST, int RT, int HPI = 1>
 static cudaError_t run_decode(const AttnArgs& a, const WsLayout& ws, const DecodeParams& p,
                               const CUtensorMap& kmap, const CUtensorMap& vmap,
                               cudaEvent_t before, cudaEvent_t after) {
-  constexpr int smem = decode_smem_bytes<D, kFp8, NST>();
-  auto kern = decode_kernel<D, kFp8, NST, RT>;
+  constexpr int smem = decode_smem_bytes<D, kFp8, NST, HPI>();
+  auto kern = decode_kernel<D, kFp8, NST, RT, HPI>;
   LaunchInfo li;
   cudaError_t e = launch_info(kern, kDecodeWarps * 32, smem, &li);
   if (e != cudaSuccess) return e;
   const int sms = li.sms, per_sm = li.per_sm;
-  const int tpt = 8 * RT / p.group;
+  const int tpt = std::max(1, 8 * RT / (p.group * HPI));
   const int64_t qtiles_max = (std::min(a.max_query_len, p.decode_max_query) + tpt - 1) / tpt;
-  const int64_t upper = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads * qtiles_max * ws.pmax;
+  const int64_t upper =
+      static_cast<int64_t>(a.num_seqs) * (a.num_kv_heads / HPI) * qtiles_max * ws.pmax;
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(upper, int64_t(sms) * per_sm));
   if (before) cudaEventRecord(before, a.stream);
   kern<<<static_cast<unsigned>(grid), kDecodeWarps * 32, smem, a.stream>>>(kmap, vmap, p);
@@ -707,6 +738,17 @@ static cudaError_t run_decode(const AttnArgs& a, const WsLayout& ws, const Decod
     e = cudaGetLastError();
   }
   return e;
+}
+
+int decode_heads_per_item(const pa_cache_desc& c, int32_t num_q_heads, int32_t num_kv_heads,
+                          int32_t max_query_len) {
+  // single-token E4M3 decode with 4 q heads per kv head fills an 8-row tile with two kv heads,
+  // whose tiles are adjacent in the pool: one 4 KiB copy each for K and V per block
+  const int G = num_kv_heads > 0 ? num_q_heads / num_kv_heads : 0;
+  return (c.cache_dtype == PA_FP8_E4M3 && c.head_dim == 128 && G == 4 && num_kv_heads % 2 == 0 &&
+          max_query_len == 1)
+             ? 2
+             : 1;
 }
 
 bool prefill_path_enabled(const pa_cache_desc& c, int32_t num_q_heads, int32_t num_kv_heads) {
@@ -738,11 +780,14 @@ cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const CUtens
   p.num_blocks = a.cache.num_blocks;
   p.max_context_len = a.max_context_len;
   p.max_query_len = a.max_query_len;
-  // An E4M3 block is half the bytes of a bf16 one: give E4M3 items twice the blocks (the
-  // workspace, sized for the bf16 choice, then holds fewer partitions than it has room for;
-  // pmax stays the row stride of the partial arrays).
+  // An E4M3 block is half the bytes of a bf16 one: give E4M3 items twice the blocks, or two
+  // kv heads (the workspace, sized for the bf16 choice, then holds fewer partitions than it has
+  // room for; pmax stays the row stride of the partial arrays).
   const bool fp8_cache = a.cache.cache_dtype == PA_FP8_E4M3;
-  p.pblk = (fp8_cache && ws.pblk <= 32) ? ws.pblk * 2 : ws.pblk;
+  const int hpi = decode_heads_per_item(a.cache, a.num_q_heads, a.num_kv_heads,
+                                        a.max_query_len);
+  p.heads_per_item = hpi;
+  p.pblk = (fp8_cache && hpi == 1 && ws.pblk <= 32) ? ws.pblk * 2 : ws.pblk;
   p.pmax = ws.pmax;
   const bool prefill = qmap != nullptr && prefill_path_enabled(a.cache, a.num_q_heads,
                                                                a.num_kv_heads);
@@ -781,7 +826,9 @@ cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const CUtens
       return e;
     if ((e = cudaEventRecord(side.join, side.stream)) != cudaSuccess) return e;
   }
-  if (fp8)
+  if (fp8 && hpi == 2)
+    e = run_decode<128, true, 2, 1, 2>(a, ws, p, kmap, vmap, before, after);
+  else if (fp8)
     e = rt2 ? run_decode<128, true, 4, 2>(a, ws, p, kmap, vmap, before, after)
             : run_decode<128, true, 4, 1>(a, ws, p, kmap, vmap, before, after);
   else if (a.head_dim == 128)

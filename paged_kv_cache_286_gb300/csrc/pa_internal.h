@@ -81,6 +81,10 @@ cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const pa_cache_desc
 // True when chunks with more than kDecodeMaxQuery queries run on the tcgen05 tile kernel
 // (bf16 pool, head_dim 128, GQA group dividing 128); otherwise every sequence takes the
 // split-KV kernel.
+// Kv heads per split-KV work item (1 or 2) for a step of this shape; the pool's tensor maps
+// then take boxes of 16 x that many rows.
+int decode_heads_per_item(const pa_cache_desc& c, int32_t num_q_heads, int32_t num_kv_heads,
+                          int32_t max_query_len);
 bool prefill_path_enabled(const pa_cache_desc& c, int32_t num_q_heads, int32_t num_kv_heads);
 
 // `qmap` (3-D view of q) is needed only when the prefill path is enabled and
