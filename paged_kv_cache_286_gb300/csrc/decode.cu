@@ -780,14 +780,15 @@ cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const CUtens
   p.num_blocks = a.cache.num_blocks;
   p.max_context_len = a.max_context_len;
   p.max_query_len = a.max_query_len;
-  // An E4M3 block is half the bytes of a bf16 one: give E4M3 items twice the blocks, or two
-  // kv heads (the workspace, sized for the bf16 choice, then holds fewer partitions than it has
-  // room for; pmax stays the row stride of the partial arrays).
+  // An E4M3 block is half the bytes of a bf16 one: give E4M3 items twice the blocks (the
+  // workspace, sized for the bf16 choice, then holds fewer partitions than it has room for;
+  // pmax stays the row stride of the partial arrays).  Fewer, longer partitions also make the
+  // merge cheaper.
   const bool fp8_cache = a.cache.cache_dtype == PA_FP8_E4M3;
   const int hpi = decode_heads_per_item(a.cache, a.num_q_heads, a.num_kv_heads,
                                         a.max_query_len);
   p.heads_per_item = hpi;
-  p.pblk = (fp8_cache && hpi == 1 && ws.pblk <= 32) ? ws.pblk * 2 : ws.pblk;
+  p.pblk = (fp8_cache && ws.pblk <= 32) ? ws.pblk * 2 : ws.pblk;
   p.pmax = ws.pmax;
   const bool prefill = qmap != nullptr && prefill_path_enabled(a.cache, a.num_q_heads,
                                                                a.num_kv_heads);
