@@ -65,6 +65,7 @@ EDGE_CTX = [1, 15, 16, 17, 32, 33, 100, 511, 512, 513, 2000]
     (4, 4, 64, "bf16"), (16, 2, 64, "bf16"),
     (8, 8, 128, "fp8_e4m3"), (16, 4, 128, "fp8_e4m3"), (32, 4, 128, "fp8_e4m3"),
     (64, 4, 128, "bf16"), (32, 2, 64, "bf16"), (64, 4, 128, "fp8_e4m3"),     # groups of 16
+    (12, 3, 128, "fp8_e4m3"),   # group of 4 over an odd number of kv heads: one head per item
 ])
 def test_decode_edge_lengths(hq, hkv, d, dtype):
     w = make_workload(EDGE_CTX, [1] * len(EDGE_CTX), num_q_heads=hq, num_kv_heads=hkv,
