@@ -185,8 +185,10 @@ struct ItemInfo {
   int s, h, qt, part, t0, n, L, nparts, blk_begin, blk_end, pos_base, rows, valid;
 };
 
+// The E4M3 two-head instance is held to 3 CTAs per SM (at most 170 registers a thread): it is
+// latency-bound, and its 2-stage rings leave room in shared memory for the third CTA.
 template <int D, bool kFp8, int NST, int RT, int HPI>
-__global__ void __launch_bounds__(kDecodeWarps * 32, 1)
+__global__ void __launch_bounds__(kDecodeWarps * 32, (kFp8 && HPI > 1) ? 3 : 1)
     decode_kernel(const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
   // RT row tiles of 8 rows: rows quad and quad + 8 of the m16 MMA (RT = 2 uses both halves).
