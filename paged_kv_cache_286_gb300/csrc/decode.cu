@@ -673,34 +673,49 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p, int32_
   for (int i = lane; i < nparts; i += 32) M = fmaxf(M, lse[i]);
 #pragma unroll
   for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  constexpr int kPer = D / 32;
+  constexpr int kPer = D / 32;  // columns per lane
+  constexpr int kBatch = 8;     // partitions whose loads are in flight together
   float acc[kPer];
 #pragma unroll
   for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
-  float wsum = 0.f;
-  const float* po = p.part_o + rid * p.pmax * D;
+  float wsum = 0.f;  // this lane's share; summed over the warp below
+  const float* po = p.part_o + rid * p.pmax * D + lane * kPer;
   for (int base = 0; base < nparts; base += 32) {
     const int i = base + lane;
     const float w = (i < nparts && M != -CUDART_INF_F) ? fast_exp2(lse[i] - M) : 0.f;
+    wsum += w;
     const int cnt = min(32, nparts - base);
-    for (int j = 0; j < cnt; ++j) {
-      const float wj = __shfl_sync(0xffffffffu, w, j);
-      wsum += wj;
-      if (wj != 0.f) {
-        const float* src = po + static_cast<int64_t>(base + j) * D + lane * kPer;
-        if constexpr (kPer == 4) {
-          const float4 v = *reinterpret_cast<const float4*>(src);
-          acc[0] += wj * v.x;
-          acc[1] += wj * v.y;
-          acc[2] += wj * v.z;
-          acc[3] += wj * v.w;
+#pragma unroll 1
+    for (int j0 = 0; j0 < cnt; j0 += kBatch) {
+      // issue the batch's loads first, then fold them in: a dependent load per partition
+      // would leave one load in flight per warp
+      float v[kBatch][kPer];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const float* src = po + static_cast<int64_t>(base + j0 + u) * D;
+        if (j0 + u < cnt) {
+          if constexpr (kPer == 4) {
+            const float4 x = *reinterpret_cast<const float4*>(src);
+            v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+          } else {
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) v[u][e] = src[e];
+          }
         } else {
 #pragma unroll
-          for (int i2 = 0; i2 < kPer; ++i2) acc[i2] += wj * src[i2];
+          for (int e = 0; e < kPer; ++e) v[u][e] = 0.f;
         }
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const float wj = __shfl_sync(0xffffffffu, w, j0 + u);  // 0 past nparts
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) acc[e] += wj * v[u][e];
       }
     }
   }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
