@@ -29,6 +29,7 @@
 #include <math_constants.h>
 
 #include <algorithm>
+#include <utility>
 
 #include "pa_common.cuh"
 #include "pa_internal.h"
@@ -97,6 +98,7 @@ __device__ __forceinline__ int prefill_items_of(const DecodeParams& p, int n, in
 // One CTA: exclusive prefix sums of decode and prefill items over sequences; resets the work
 // counters and flags inconsistent lengths.
 __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
+  grid_launch_dependents();  // the attention kernel may set up its CTAs meanwhile
   __shared__ int2 warp_sums[32];
   __shared__ int2 carry_s;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -219,6 +221,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (kFp8 && HPI > 1) ? 3 : 1)
     prefetch_tensormap(&vmap);
   }
   __syncthreads();
+  grid_dependency_wait();  // the plan (and everything before it on the stream) is complete
 
   const int total_items = p.item_start[p.num_seqs];
   uint32_t it = 0;          // blocks this warp has consumed so far (stage / phase tracking)
@@ -652,6 +655,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (kFp8 && HPI > 1) ? 3 : 1)
 // One warp per (token, q head) row of a sequence that was split into several partitions.
 template <int D>
 __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p, int32_t num_tokens) {
+  grid_dependency_wait();  // the attention kernel's partials are complete
   const int lane = threadIdx.x & 31;
   const int64_t rid = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   if (rid >= static_cast<int64_t>(num_tokens) * p.num_q_heads) return;
@@ -727,6 +731,24 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p, int32_
   }
 }
 
+// Launch with programmatic stream serialization: the kernel may start while the previous kernel
+// of the stream finishes, and waits (grid_dependency_wait) before reading its results.
+template <typename... Params, typename... Args>
+static cudaError_t launch_dependent(void (*kern)(Params...), dim3 grid, dim3 block, int smem,
+                                    cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 template <int D, bool kFp8, int NST, int RT, int HPI = 1>
 static cudaError_t run_decode(const AttnArgs& a, const WsLayout& ws, const DecodeParams& p,
                               const CUtensorMap& kmap, const CUtensorMap& vmap,
@@ -743,16 +765,16 @@ static cudaError_t run_decode(const AttnArgs& a, const WsLayout& ws, const Decod
       static_cast<int64_t>(a.num_seqs) * (a.num_kv_heads / HPI) * qtiles_max * ws.pmax;
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(upper, int64_t(sms) * per_sm));
   if (before) cudaEventRecord(before, a.stream);
-  kern<<<static_cast<unsigned>(grid), kDecodeWarps * 32, smem, a.stream>>>(kmap, vmap, p);
+  e = launch_dependent(kern, dim3(static_cast<unsigned>(grid)), dim3(kDecodeWarps * 32), smem,
+                       a.stream, kmap, vmap, p);
   if (after) cudaEventRecord(after, a.stream);
-  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (ws.pmax > 1) {
     const int64_t rows = static_cast<int64_t>(a.num_q_tokens) * a.num_q_heads;
     const int64_t blocks = (rows + 7) / 8;
     if (blocks > 0)
-      merge_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, a.stream>>>(p, a.num_q_tokens);
-    e = cudaGetLastError();
+      e = launch_dependent(merge_kernel<D>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                           a.stream, p, a.num_q_tokens);
   }
   return e;
 }
