@@ -60,8 +60,8 @@ pa_status encode_pool_map(CUtensorMap* map, const void* base, const pa_cache_des
   auto enc = tensor_map_encoder();
   if (!enc) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const bool fp8 = c.cache_dtype == PA_FP8_E4M3;
-  const cuuint64_t rows =
-      static_cast<cuuint64_t>(c.num_blocks) * c.num_kv_heads * static_cast<cuuint64_t>(c.block_size);
+  const cuuint64_t rows = static_cast<cuuint64_t>(c.num_blocks) * c.num_kv_heads *
+                          static_cast<cuuint64_t>(c.block_size);
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(c.head_dim), rows};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(c.head_dim) * (fp8 ? 1 : 2)};
   const cuuint32_t box[2] = {fp8 ? 128u : 64u,
@@ -112,8 +112,8 @@ pa_status check_cache_desc(const pa_cache_desc* c, bool for_attention) {
     const bool ok = c->cache_dtype == PA_FP8_E4M3 ? c->head_dim == 128
                                                   : (c->head_dim == 64 || c->head_dim == 128);
     if (!ok)
-      return fail(PA_ERR_UNSUPPORTED, "attention over head_dim %d with this cache dtype is not built",
-                  c->head_dim);
+      return fail(PA_ERR_UNSUPPORTED,
+                  "attention over head_dim %d with this cache dtype is not built", c->head_dim);
   }
   const double rows = double(c->num_blocks) * c->num_kv_heads * c->block_size;
   if (rows >= 4294967296.0 || rows * c->head_dim >= 9.2e18)

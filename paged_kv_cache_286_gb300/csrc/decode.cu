@@ -12,17 +12,20 @@
 //    tiles (both halves of the MMA's M) serve groups above 8 and multi-token runs of up to 16
 //    rows; single-token decode keeps 8-row tiles, the cheaper instance.  Runs with more rows
 //    (long chunks, speculative verify with GQA) go to the tensor-core prefill tiles when those
-//    are built for the pool, and otherwise take several tiles here.  A plan kernel turns context lengths into per-sequence item counts; the
-//    attention kernel is persistent and takes items from an atomic counter.
+//    are built for the pool, and otherwise take several tiles here.  Single-token E4M3 decode
+//    with 4 q heads per kv head takes two kv heads per item, filling the 8 rows.
+//  * A plan kernel turns context lengths into per-sequence item counts; the attention kernel is
+//    persistent, takes items from an atomic counter, and starts its CTAs while the plan runs
+//    (programmatic dependent launch).
 //  * Each of the CTA's 4 warps owns every 4th block of the partition and streams it through its
 //    own ring of shared-memory stages: one lane issues 2-D TMA tile copies of the (block, head)
 //    K and V tiles (128-byte swizzle) after reading the block id from the table, completion is
 //    counted on the stage's mbarrier.  The HBM stream is the whole cost of decode.
 //  * Scores and P.V run on warp-level tensor-core MMAs (m16n8k16): S = Q K^T with the rows as M
-//    (an 8-row tile pads M to 16), and O^T = V^T P^T so that the probabilities feed the second MMA straight
-//    from the first one's accumulators.  bf16 caches: P is split into bf16 hi + lo parts, which
-//    keeps P exact to ~2^-16.  E4M3 caches: K and V are converted to f16 in registers (exact),
-//    q is scaled by a power of two per row into f16 range, P is f16.
+//    (an 8-row tile pads M to 16), and O^T = V^T P^T so that the probabilities feed the second
+//    MMA straight from the first one's accumulators.  bf16 caches: P is split into bf16 hi + lo
+//    parts, which keeps P exact to ~2^-16.  E4M3 caches: K and V are converted to f16 in
+//    registers (exact), q is scaled by a power of two per row into f16 range, P is f16.
 //  * Online softmax in the log2 domain per warp; the 4 warps' (m, l, O) are merged in shared
 //    memory; an item that covers the whole sequence writes `out`, otherwise it writes a
 //    normalised partial and its log-sum-exp, which the merge kernel combines.
