@@ -333,3 +333,42 @@ def test_step_replays_from_a_cuda_graph():
         graph.replay()
     torch.cuda.synchronize()
     assert torch.equal(d.out, out_eager)
+
+
+def test_concurrent_callers_on_their_own_streams():
+    """Two host threads run attention steps with prefill chunks (which fork the prefill tiles to
+    a per-thread side stream) on their own streams and workspaces over one shared pool; each
+    result equals the single-caller one bitwise."""
+    import threading
+    import paged_kv_cache_286_gb300 as pa
+    h = _h()
+    w = make_workload([300, 1000, 2500, 40], [1, 1, 37, 1], num_q_heads=16, num_kv_heads=4,
+                      head_dim=128, seed=321)
+    d, ref = h.run_gpu(w)
+    ref = ref.clone()
+    outs, errors = {}, []
+
+    def caller(tag):
+        try:
+            stream = torch.cuda.Stream()
+            ws = pa.new_workspace(d.ws.numel())
+            out = torch.empty_like(d.out)
+            with torch.cuda.stream(stream):
+                for _ in range(5):
+                    pa.attention(d.q, d.k_cache, d.v_cache, d.tables, d.ctx, d.qsl, ws,
+                                 scale=w.scale, max_context_len=w.max_context_len,
+                                 max_query_len=w.max_query_len, out=out, stream=stream)
+            stream.synchronize()
+            assert pa.check_error(ws, stream=stream) == 0
+            outs[tag] = out
+        except Exception as e:  # surfaced below
+            errors.append(e)
+
+    threads = [threading.Thread(target=caller, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for tag in (0, 1):
+        assert torch.equal(outs[tag], ref)
