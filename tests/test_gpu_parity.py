@@ -186,15 +186,16 @@ def test_e4m3_append_every_bf16_value(scale):
 
 
 # ---- invariants on the GPU ---------------------------------------------------------------
-def test_block_permutation_is_bitwise_invariant():
+@pytest.mark.parametrize("dtype", ["bf16", "fp8_e4m3"])
+def test_block_permutation_is_bitwise_invariant(dtype):
     h = _h()
     w = make_workload([300, 1000, 17, 4000], [1, 1, 1, 1], num_q_heads=16, num_kv_heads=4,
-                      head_dim=128, seed=9, pool_factor=1.5)
+                      head_dim=128, seed=9, pool_factor=1.5, cache_dtype=dtype)
     d1, out1 = h.run_gpu(w)
     out1 = out1.clone()
     perm = np.random.default_rng(1).permutation(w.num_blocks)
     w2 = make_workload([300, 1000, 17, 4000], [1, 1, 1, 1], num_q_heads=16, num_kv_heads=4,
-                       head_dim=128, seed=9, pool_factor=1.5)
+                       head_dim=128, seed=9, pool_factor=1.5, cache_dtype=dtype)
     w2.block_tables = np.where(w.block_tables >= 0, perm[np.maximum(w.block_tables, 0)], -1) \
         .astype(np.int32)
     w2.slot_mapping = perm[w.slot_mapping // 16] * 16 + w.slot_mapping % 16
@@ -203,11 +204,12 @@ def test_block_permutation_is_bitwise_invariant():
     assert torch.equal(out1, out2)
 
 
-def test_shared_prefix_equals_duplicated_prefix_bitwise():
+@pytest.mark.parametrize("dtype", ["bf16", "fp8_e4m3"])
+def test_shared_prefix_equals_duplicated_prefix_bitwise(dtype):
     h = _h()
     ctx = [2000, 1700, 1300]
     w = make_workload(ctx, [1, 1, 1], num_q_heads=8, num_kv_heads=2, head_dim=128, seed=10,
-                      shared_prefix_blocks=20, pool_factor=2.0)
+                      shared_prefix_blocks=20, pool_factor=2.0, cache_dtype=dtype)
     d, out_shared = h.run_gpu(w)
     out_shared = out_shared.clone()
     # duplicate the 20 shared blocks into private copies for sequences 1 and 2
