@@ -374,3 +374,24 @@ def test_concurrent_callers_on_their_own_streams():
     assert not errors, errors
     for tag in (0, 1):
         assert torch.equal(outs[tag], ref)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8_e4m3"])
+def test_poisoned_workspace_gives_the_same_output(dtype):
+    """Every byte of the workspace past its header filled with 0xFF (fp32 NaN) before the step:
+    the partials, item tables and plan arrays are all written before they are read, so the
+    output equals the one from a clean workspace bitwise."""
+    import paged_kv_cache_286_gb300 as pa
+    h = _h()
+    w = make_workload([5000, 3100, 700, 1], [1, 1, 1, 1], num_q_heads=8, num_kv_heads=2,
+                      head_dim=128, seed=77, cache_dtype=dtype)
+    d, ref = h.run_gpu(w)
+    ref = ref.clone()
+    ws = pa.new_workspace(d.ws.numel())
+    ws[pa.PA_WORKSPACE_HEADER_BYTES:].fill_(255)
+    out = torch.full_like(d.out, float("nan"))
+    pa.attention(d.q, d.k_cache, d.v_cache, d.tables, d.ctx, d.qsl, ws, scale=w.scale,
+                 max_context_len=w.max_context_len, max_query_len=w.max_query_len, out=out,
+                 k_scale=w.k_scale, v_scale=w.v_scale)
+    assert pa.check_error(ws) == 0
+    assert torch.equal(out, ref)
