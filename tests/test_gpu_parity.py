@@ -92,6 +92,9 @@ def test_multi_query_causal(qlens, ctx, dtype):
     (64, 4, [1, 2, 5, 16], [33, 1000, 5, 300]),       # group of 16: one token per tile
     (32, 2, [100, 1, 40], [2000, 77, 40]),            # group of 16 with long chunks
     (24, 8, [7, 2, 11], [7, 260, 900]),               # group of 3: 5 tokens (15 rows) a tile
+    (16, 2, [3, 2, 1], [70, 900, 33]),                # group of 8: 24 rows to the tensor-core
+                                                      # tiles, 16 and 8 rows to the split-KV path
+    (8, 4, [9, 8, 1], [9, 500, 1200]),                # group of 2: 18 rows vs 16
 ])
 @pytest.mark.parametrize("dtype", ["bf16", "fp8_e4m3"])
 def test_multi_query_row_tiles(hq, hkv, qlens, ctx, dtype):
