@@ -143,7 +143,13 @@ size_t pa_attention_workspace_size(int32_t num_seqs, int32_t num_q_tokens, int32
  *   workspace     device buffer of workspace_bytes >= pa_attention_workspace_size(...); its
  *                 first PA_WORKSPACE_HEADER_BYTES hold the error word.
  * A sequence with n_s == 0 produces nothing.  Accumulation is fp32; scores use exp2 of
- * log2(e)-prescaled logits. */
+ * log2(e)-prescaled logits.
+ * Streams: with a bf16 pool of head_dim 128, query runs of more than 16 tokens or more than 16
+ * (token x q head) rows are computed by a tensor-core kernel on a high-priority side stream of
+ * the calling thread, forked from `stream` by an event and joined back into it before the call
+ * returns, so all of the call's work stays ordered on `stream` (and is captured with it into a
+ * CUDA graph).  The first such call of a thread on a device creates that stream and its two
+ * events; make it before any stream capture. */
 pa_status pa_attention(const void* q, int32_t num_q_tokens, const void* k_cache,
                        const void* v_cache, const pa_cache_desc* cache,
                        const int32_t* block_tables, int32_t max_blocks_per_seq,
