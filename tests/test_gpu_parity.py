@@ -398,3 +398,24 @@ def test_poisoned_workspace_gives_the_same_output(dtype):
                  k_scale=w.k_scale, v_scale=w.v_scale)
     assert pa.check_error(ws) == 0
     assert torch.equal(out, ref)
+
+
+def test_pipelined_host_loop_reads_back_every_step_output():
+    """bench.py's end-to-end loop (packed inputs copied in, output copied back, double-buffered
+    against the compute on a copy stream) hands back the step's output in both host buffers."""
+    import os
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    w = make_config(4)
+    dw = bench.DeviceWorkload(w, torch.device("cuda", 0))
+    dw.step()
+    torch.cuda.synchronize()
+    ref = dw.out.cpu()
+    for t in (dw.out, dw.out2):
+        t.fill_(float("nan"))
+    for t in (dw.out_host, dw.out_host2):
+        t.fill_(float("nan"))
+    dw.steps_from_host(4, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert torch.equal(dw.out_host, ref) and torch.equal(dw.out_host2, ref)
