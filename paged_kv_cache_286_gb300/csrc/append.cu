@@ -17,6 +17,8 @@ __global__ void __launch_bounds__(256) cache_append_kernel(
     int32_t num_tokens, int32_t num_kv_heads, int32_t vec_per_row, int64_t total_slots,
     void* __restrict__ k_cache, void* __restrict__ v_cache, float k_scale, float v_scale,
     uint32_t* __restrict__ err) {
+  grid_dependency_wait();    // launched early (programmatic dependent launch): inputs ready
+  grid_launch_dependents();  // the step's plan kernel may launch meanwhile
   const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t per_token = static_cast<int64_t>(num_kv_heads) * vec_per_row;
   if (gid >= per_token * num_tokens) return;
@@ -71,16 +73,16 @@ cudaError_t launch_cache_append(const void* k, const void* v, const int64_t* slo
   const int64_t grid = (threads + block - 1) / block;
   const int64_t total_slots = static_cast<int64_t>(c.num_blocks) * c.block_size;
   if (c.cache_dtype == PA_FP8_E4M3) {
-    cache_append_kernel<true><<<static_cast<unsigned>(grid), block, 0, stream>>>(
-        static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, num_tokens,
-        c.num_kv_heads, vec_per_row, total_slots, k_cache, v_cache, c.k_scale, c.v_scale,
-        err);
-  } else {
-    cache_append_kernel<false><<<static_cast<unsigned>(grid), block, 0, stream>>>(
-        static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, num_tokens,
-        c.num_kv_heads, vec_per_row, total_slots, k_cache, v_cache, 1.f, 1.f, err);
+    return launch_dependent(cache_append_kernel<true>, dim3(static_cast<unsigned>(grid)),
+                            dim3(block), 0, stream, static_cast<const uint4*>(k),
+                            static_cast<const uint4*>(v), slots, num_tokens, c.num_kv_heads,
+                            vec_per_row, total_slots, k_cache, v_cache, c.k_scale, c.v_scale,
+                            err);
   }
-  return cudaGetLastError();
+  return launch_dependent(cache_append_kernel<false>, dim3(static_cast<unsigned>(grid)),
+                          dim3(block), 0, stream, static_cast<const uint4*>(k),
+                          static_cast<const uint4*>(v), slots, num_tokens, c.num_kv_heads,
+                          vec_per_row, total_slots, k_cache, v_cache, 1.f, 1.f, err);
 }
 
 }  // namespace pa

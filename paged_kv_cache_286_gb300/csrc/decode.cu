@@ -101,6 +101,7 @@ __device__ __forceinline__ int prefill_items_of(const DecodeParams& p, int n, in
 // One CTA: exclusive prefix sums of decode and prefill items over sequences; resets the work
 // counters and flags inconsistent lengths.
 __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
+  grid_dependency_wait();    // whatever the stream ran before (the step's append) is complete
   grid_launch_dependents();  // the attention kernel may set up its CTAs meanwhile
   __shared__ int2 warp_sums[32];
   __shared__ int2 carry_s;
@@ -734,24 +735,6 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p, int32_
   }
 }
 
-// Launch with programmatic stream serialization: the kernel may start while the previous kernel
-// of the stream finishes, and waits (grid_dependency_wait) before reading its results.
-template <typename... Params, typename... Args>
-static cudaError_t launch_dependent(void (*kern)(Params...), dim3 grid, dim3 block, int smem,
-                                    cudaStream_t stream, Args&&... args) {
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
-}
-
 template <int D, bool kFp8, int NST, int RT, int HPI = 1>
 static cudaError_t run_decode(const AttnArgs& a, const WsLayout& ws, const DecodeParams& p,
                               const CUtensorMap& kmap, const CUtensorMap& vmap,
@@ -850,8 +833,7 @@ cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const CUtens
   const bool rt2 = p.group > 8 || (!mixed && static_cast<int64_t>(dec_q) * p.group > 8);
   p.rows_per_tile = rt2 ? 16 : 8;
 
-  plan_kernel<<<1, 1024, 0, a.stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_dependent(plan_kernel, dim3(1), dim3(1024), 0, a.stream, p);
   if (e != cudaSuccess) return e;
   // The prefill tiles (tensor pipe, key slices mostly from L2) and the split-KV decode (HBM)
   // run side by side: the prefill kernel goes to a high-priority side stream forked from the

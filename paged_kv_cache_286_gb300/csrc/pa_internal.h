@@ -2,9 +2,11 @@
 #pragma once
 
 #include <cuda.h>
-#include <cuda_runtime_api.h>
+#include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
+
+#include <utility>
 
 #include "pa.h"
 
@@ -89,6 +91,24 @@ bool prefill_path_enabled(const pa_cache_desc& c, int32_t num_q_heads, int32_t n
 
 // `qmap` (3-D view of q) is needed only when the prefill path is enabled and
 // max_query_len > kDecodeMaxQuery; it may be NULL otherwise.
+// Launch with programmatic stream serialization: the kernel may start while the previous kernel
+// of the stream finishes, and waits (grid_dependency_wait) before reading its results.
+template <typename... Params, typename... Args>
+inline cudaError_t launch_dependent(void (*kern)(Params...), dim3 grid, dim3 block, int smem,
+                                    cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, const CUtensorMap* qmap,
                              cudaEvent_t before, cudaEvent_t after);
