@@ -32,6 +32,7 @@
 #include <math_constants.h>
 
 #include <algorithm>
+#include <climits>
 #include <utility>
 
 #include "pa_common.cuh"
@@ -656,20 +657,77 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (kFp8 && HPI > 1) ? 3 : 1)
   }
 }
 
+// Eight loads of kPer consecutive floats each, issued back to back in one asm block (so that
+// they are in flight together whatever the register allocator prefers); the merge issues two
+// such blocks before it uses any of the sixteen results.
+template <int kPer>
+__device__ __forceinline__ void load_batch8(const float* const (&src)[8], float (&v)[8][kPer]);
+
+template <>
+__device__ __forceinline__ void load_batch8<4>(const float* const (&src)[8], float (&v)[8][4]) {
+  asm volatile(
+      "ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%32];\n\t"
+      "ld.global.nc.v4.f32 {%4, %5, %6, %7}, [%33];\n\t"
+      "ld.global.nc.v4.f32 {%8, %9, %10, %11}, [%34];\n\t"
+      "ld.global.nc.v4.f32 {%12, %13, %14, %15}, [%35];\n\t"
+      "ld.global.nc.v4.f32 {%16, %17, %18, %19}, [%36];\n\t"
+      "ld.global.nc.v4.f32 {%20, %21, %22, %23}, [%37];\n\t"
+      "ld.global.nc.v4.f32 {%24, %25, %26, %27}, [%38];\n\t"
+      "ld.global.nc.v4.f32 {%28, %29, %30, %31}, [%39];"
+      : "=f"(v[0][0]), "=f"(v[0][1]), "=f"(v[0][2]), "=f"(v[0][3]), "=f"(v[1][0]),
+        "=f"(v[1][1]), "=f"(v[1][2]), "=f"(v[1][3]), "=f"(v[2][0]), "=f"(v[2][1]),
+        "=f"(v[2][2]), "=f"(v[2][3]), "=f"(v[3][0]), "=f"(v[3][1]), "=f"(v[3][2]),
+        "=f"(v[3][3]), "=f"(v[4][0]), "=f"(v[4][1]), "=f"(v[4][2]), "=f"(v[4][3]),
+        "=f"(v[5][0]), "=f"(v[5][1]), "=f"(v[5][2]), "=f"(v[5][3]), "=f"(v[6][0]),
+        "=f"(v[6][1]), "=f"(v[6][2]), "=f"(v[6][3]), "=f"(v[7][0]), "=f"(v[7][1]),
+        "=f"(v[7][2]), "=f"(v[7][3])
+      : "l"(src[0]), "l"(src[1]), "l"(src[2]), "l"(src[3]), "l"(src[4]), "l"(src[5]),
+        "l"(src[6]), "l"(src[7]));
+}
+
+template <>
+__device__ __forceinline__ void load_batch8<2>(const float* const (&src)[8], float (&v)[8][2]) {
+  asm volatile(
+      "ld.global.nc.v2.f32 {%0, %1}, [%16];\n\t"
+      "ld.global.nc.v2.f32 {%2, %3}, [%17];\n\t"
+      "ld.global.nc.v2.f32 {%4, %5}, [%18];\n\t"
+      "ld.global.nc.v2.f32 {%6, %7}, [%19];\n\t"
+      "ld.global.nc.v2.f32 {%8, %9}, [%20];\n\t"
+      "ld.global.nc.v2.f32 {%10, %11}, [%21];\n\t"
+      "ld.global.nc.v2.f32 {%12, %13}, [%22];\n\t"
+      "ld.global.nc.v2.f32 {%14, %15}, [%23];"
+      : "=f"(v[0][0]), "=f"(v[0][1]), "=f"(v[1][0]), "=f"(v[1][1]), "=f"(v[2][0]),
+        "=f"(v[2][1]), "=f"(v[3][0]), "=f"(v[3][1]), "=f"(v[4][0]), "=f"(v[4][1]),
+        "=f"(v[5][0]), "=f"(v[5][1]), "=f"(v[6][0]), "=f"(v[6][1]), "=f"(v[7][0]),
+        "=f"(v[7][1])
+      : "l"(src[0]), "l"(src[1]), "l"(src[2]), "l"(src[3]), "l"(src[4]), "l"(src[5]),
+        "l"(src[6]), "l"(src[7]));
+}
+
 // One warp per (token, q head) row of a sequence that was split into several partitions.
 template <int D>
-__global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p, int32_t num_tokens) {
+// (At least 2 CTAs per SM, i.e. up to 128 registers a thread: room for the sixteen loads in
+// flight, which a full-occupancy register budget of 32 would serialise.)
+__global__ void __launch_bounds__(256, 2)
+    merge_kernel(const DecodeParams p, int32_t num_tokens) {
   grid_dependency_wait();  // the attention kernel's partials are complete
   const int lane = threadIdx.x & 31;
   const int64_t rid = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   if (rid >= static_cast<int64_t>(num_tokens) * p.num_q_heads) return;
   const int t = static_cast<int>(rid / p.num_q_heads);
-  int lo = 0, hi = p.num_seqs;  // sequence of token t: largest s with qsl[s] <= t
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (p.qsl[mid] <= t) lo = mid; else hi = mid;
+  // sequence of token t, the largest s with qsl[s] <= t (qsl is non-decreasing, qsl[0] = 0):
+  // a 32-way search by the warp, one coalesced load per round
+  int lo = 0, span = p.num_seqs;
+  while (span > 32) {
+    const int step = (span + 31) >> 5;
+    const int idx = lo + lane * step;
+    const int start = idx < lo + span ? p.qsl[idx] : INT_MAX;
+    const int last = 31 - __clz(__ballot_sync(0xffffffffu, start <= t));
+    lo += last * step;
+    span = min(step, span - last * step);
   }
-  const int s = lo;
+  const int start = lane < span ? p.qsl[lo + lane] : INT_MAX;
+  const int s = lo + 31 - __clz(__ballot_sync(0xffffffffu, start <= t));
   const int n = p.qsl[s + 1] - p.qsl[s];
   const int L = p.context_lens[s];
   bool bad;
@@ -682,7 +740,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p, int32_
 #pragma unroll
   for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   constexpr int kPer = D / 32;  // columns per lane
-  constexpr int kBatch = 8;     // partitions whose loads are in flight together
+  constexpr int kBatch = 16;    // partitions whose loads are in flight together
   float acc[kPer];
 #pragma unroll
   for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
@@ -698,22 +756,14 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p, int32_
       // issue the batch's loads first, then fold them in: a dependent load per partition
       // would leave one load in flight per warp
       float v[kBatch][kPer];
+      // past the last partition a load repeats it (a written, finite partial) under a zero
+      // weight, so the batch's loads are unconditional and go out back to back
+      const float* src[2][8];
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const float* src = po + static_cast<int64_t>(base + j0 + u) * D;
-        if (j0 + u < cnt) {
-          if constexpr (kPer == 4) {
-            const float4 x = *reinterpret_cast<const float4*>(src);
-            v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
-          } else {
-#pragma unroll
-            for (int e = 0; e < kPer; ++e) v[u][e] = src[e];
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < kPer; ++e) v[u][e] = 0.f;
-        }
-      }
+      for (int u = 0; u < kBatch; ++u)
+        src[u >> 3][u & 7] = po + static_cast<int64_t>(base + min(j0 + u, cnt - 1)) * D;
+      load_batch8<kPer>(src[0], *reinterpret_cast<float(*)[8][kPer]>(&v[0][0]));
+      load_batch8<kPer>(src[1], *reinterpret_cast<float(*)[8][kPer]>(&v[8][0]));
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
         const float wj = __shfl_sync(0xffffffffu, w, j0 + u);  // 0 past nparts
