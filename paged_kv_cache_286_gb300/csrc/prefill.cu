@@ -16,20 +16,29 @@
 //    boxes), then for every 128 keys the 8 (block, kv head) K tiles of the block table; warp 6
 //    does the same for the V tiles.  Eight lanes of each issue one block's boxes apiece, into
 //    three-stage K and V rings (128-byte swizzle, completion on mbarriers).
-//  * Warp 1 issues tcgen05.mma from one thread: S = Q K^T into one of two TMEM buffers
-//    (128 x 128 fp32), and O += P V into a third, with P read from TMEM and V from shared
-//    memory (MN-major).  The softmax threads write P back over their S buffer as bf16 hi and lo
-//    halves (64 columns each), so P V is exact to ~2^-16 like the decode path, and the next
-//    tile's softmax can run while this tile's P V is in flight.
-//  * Warps 2-5 own one row each: they read the row of S from TMEM once, mask keys beyond the
-//    row's position, keep the running max in the log2 domain and rescale O in TMEM only when
-//    the max grows by more than 2^8 (the final division uses the same max, so the result is
-//    exact), and finally divide O by the row sum and store it.
+//  * Warp 1 issues tcgen05.mma from one thread: S = Q K^T into one of three TMEM buffers
+//    (128 x 128 fp32), and O += P V into a fourth, with P read from TMEM and V from shared
+//    memory (MN-major).  The softmax threads write P back over their S columns as bf16 hi and
+//    lo parts (keys 0-63: hi in columns 0-31, lo in 32-63; keys 64-127 likewise in 64-127), so
+//    P V is exact to ~2^-16 like the decode path, and the next tile's softmax can run while
+//    this tile's P V is in flight.
+//  * Softmax, one thread per row (TMEM lane): it reads its row of S from TMEM once, masks keys
+//    beyond the row's position, keeps the running max in the log2 domain and rescales O in
+//    TMEM only when the max grows by more than 2^8 (the final division uses the same max, so
+//    the result is exact), and finally divides O by the row sum and stores it.  Warps 2-5 do
+//    this for whole rows.  When every run has at most 64 rows (speculative verify), at most
+//    two of the four lane quarters hold rows, and the kernel instance with the row split runs
+//    instead: warps 2-5 take keys (and O columns) 0-63 and warps 7-10 keys 64-127, the two
+//    threads of a row agreeing on its max, and at the end adding their sums, through a
+//    shared-memory slot and an mbarrier of the pair.  A warp can only reach the lane quarter
+//    of its own SM sub-partition, so the split puts a second warp on each busy sub-partition
+//    to hide the latency of the exponentials and TMEM traffic.
 //  * V rows past the last valid key (stale slots, possibly NaN) are zeroed in shared memory
 //    before P V reads them; K there only feeds masked scores.
 #include <math_constants.h>
 
 #include <algorithm>
+#include <climits>
 
 #include "pa_common.cuh"
 #include "pa_internal.h"
@@ -45,9 +54,18 @@ constexpr int kHalf = 16384;  // one 64-column region of a 128-row bf16 tile
 constexpr int kTile = 32768;  // 128 x 128 bf16
 constexpr int kQ = 0, kK = kTile, kV = kK + kStages * kTile;
 constexpr int kCtl = kV + kStages * kTile;  // control block (barriers, item, flags)
-constexpr int kSmem = 1024 + kCtl + 256;
-constexpr int kThreads = 224;
+constexpr int kXBar = kCtl + 256;           // 4 mbarriers: one per pair of softmax warps
+constexpr int kXSlot = kXBar + 32;          // 3 x 128 row slots of the pairs' exchanges
+constexpr int kXBufs = 3;
 constexpr int kVWarp = 6;     // V producer (warp 0 loads q and K)
+// Without the row split: warps 2-5 are the softmax, a thread a whole row.  With it: warps 2-5
+// take keys 0-63 of their rows and warps 7-10 keys 64-127, and the pairs exchange row sums
+// and maxima through shared memory.
+__host__ __device__ constexpr int threads(bool split) { return split ? 352 : 224; }
+__host__ __device__ constexpr int softmax_threads(bool split) { return split ? 256 : 128; }
+__host__ __device__ constexpr int smem_bytes(bool split) {
+  return 1024 + (split ? kXSlot + kXBufs * kRows * 4 : kCtl + 256);
+}
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = kSBufs * 128;
 constexpr float kRescaleLog2 = 8.f;
@@ -84,8 +102,20 @@ struct PfCtl {
   PfItem item;
 };
 static_assert(sizeof(PfCtl) <= 256, "control block too large");
+static_assert(pf::smem_bytes(true) <= 232448, "more shared memory than a CTA may have");
 
-__global__ void __launch_bounds__(pf::kThreads, 1)
+// Floats mapped to ints of the same order (an involution), so that integer atomicMax takes the
+// max of floats.  The empty slot INT_MIN is below every mapped float and reads as -0.0f.
+__device__ __forceinline__ int float_order_key(float f) {
+  const int i = __float_as_int(f);
+  return i >= 0 ? i : (i ^ 0x7fffffff);
+}
+__device__ __forceinline__ float order_key_float(int k) {
+  return __int_as_float(k >= 0 ? k : (k ^ 0x7fffffff));
+}
+
+template <bool kSplit>
+__global__ void __launch_bounds__(pf::threads(kSplit), 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
@@ -107,15 +137,21 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     // S of tile g+3 is issued only after P V of tile g, which waits for P of tile g
     for (int i = 0; i < pf::kSBufs; ++i) {
       mbar_init(&ctl->s_full[i], 1);
-      mbar_init(&ctl->p_full[i], pf::kRows);
+      mbar_init(&ctl->p_full[i], pf::softmax_threads(kSplit));
       mbar_init(&ctl->o_done[i], 1);
     }
+    if (kSplit)
+      for (int q = 0; q < 4; ++q)
+        mbar_init(reinterpret_cast<uint64_t*>(smem + pf::kXBar) + q, 2);  // one lane a warp
     ctl->abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&qmap);
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
   }
+  int* xslot = reinterpret_cast<int*>(smem + pf::kXSlot);  // [kXBufs][kRows], split only
+  if (kSplit)
+    for (int i = tid; i < pf::kXBufs * pf::kRows; i += pf::threads(true)) xslot[i] = INT_MIN;
   if (warp == 1) tmem_alloc(&ctl->tmem_base, pf::kTmemCols);
   tc_fence_before();
   __syncthreads();
@@ -124,6 +160,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
   const int total = p.item_start[p.num_seqs];
   uint32_t tc = 0;  // KV tiles processed by this CTA so far (ring / phase tracking)
   uint32_t ic = 0;  // items processed by this CTA so far
+  uint32_t xc = 0;  // exchanges of this softmax thread's pair so far (slot / phase tracking)
   const int G = p.group;
   const int tpt = pf::kRows / G;  // query tokens per tile
 
@@ -308,15 +345,17 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         tc_fence_after();
         if (lane == 0) {
           const uint32_t v_addr = smem_u32(vt);
-          const uint32_t p_hi = tmem + b * 128u, p_lo = p_hi + 64u;
+          // P of keys 16 ks .. 16 ks + 15: the hi parts of keys 0-63 in columns 0-31 of the
+          // buffer and their lo parts in 32-63; keys 64-127 the same in columns 64-127
+          auto p_col = [&](int ks) { return tmem + b * 128u + (ks >> 2) * 64u + (ks & 3) * 8u; };
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            tc_mma_bf16_ts(tmem + pf::kOCol, p_hi + ks * 8,
+            tc_mma_bf16_ts(tmem + pf::kOCol, p_col(ks),
                            smem_desc_sw128(v_addr + ks * 2048, pf::kHalf, 1024), id_pv,
                            j > 0 || ks > 0);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            tc_mma_bf16_ts(tmem + pf::kOCol, p_lo + ks * 8,
+            tc_mma_bf16_ts(tmem + pf::kOCol, p_col(ks) + 32u,
                            smem_desc_sw128(v_addr + ks * 2048, pf::kHalf, 1024), id_pv, true);
           tc_commit(&ctl->o_done[b]);
           tc_commit(&ctl->v_empty[st]);
@@ -328,56 +367,89 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       }
     } else {
       // ------------------------------------------------------------- softmax rows -------
+      constexpr int kC = kSplit ? 64 : 128;  // keys (and O columns) of a thread
+      const int half = (kSplit && warp > pf::kVWarp) ? 1 : 0;
       const int quarter = warp & 3;        // TMEM lane quarter this warp may access
       const int r = quarter * 32 + lane;   // tile row = TMEM lane
       const int tok = r / G;
       const bool row_ok = tok < I.ntok;
       const int row_pos = I.pos0 + tok;
       const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+      const uint32_t hc = half * 64u;      // first S / P / O column of this thread
+      uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + pf::kXBar) + quarter;
+      // Combine v with the other half of the row (max, or sum): both threads fold v into the
+      // row's slot, the two warps meet at the pair's barrier (lane 0 of each arrives once the
+      // warp's updates are ordered before it) and read the slot; then the slot that the
+      // exchange after next uses is cleared (its last readers have passed this barrier).
+      auto exchange = [&](float v, bool sum, float* out) -> bool {
+        if (!kSplit) {
+          *out = v;
+          return true;
+        }
+        int* slot = xslot + (xc % pf::kXBufs) * pf::kRows + r;
+        if (sum) atomicAdd(reinterpret_cast<float*>(slot), v);  // -0.0f + a + b, either order
+        else atomicMax(slot, float_order_key(v));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xbar);
+        if (!wait(xbar, xc & 1u)) return false;
+        const int k = *reinterpret_cast<volatile int*>(slot);
+        *out = sum ? __int_as_float(k) : order_key_float(k);
+        xslot[((xc + 2) % pf::kXBufs) * pf::kRows + r] = INT_MIN;
+        ++xc;
+        return true;
+      };
+      // a quarter with no row of the run writes P = 0 and skips the exchanges (both warps of
+      // a pair see the same rows)
+      const bool live = __any_sync(0xffffffffu, row_ok);
       float m_used = 0.f, l = 0.f;
       bool ok = true;
       for (int j = 0; j < I.nkv; ++j) {
         const uint32_t g = tc + j, b = g % pf::kSBufs;
         if (!(ok = wait(&ctl->s_full[b], (g / pf::kSBufs) & 1u))) break;
         tc_fence_after();
-        const int kmax = row_ok ? row_pos - j * pf::kKeys : -1;  // keys 0..kmax are visible
-        if (!__any_sync(0xffffffffu, row_ok)) {  // a quarter of rows past the run: P = 0
+        const uint32_t sb = tl + b * 128u + hc;  // this thread's columns of S, then of P
+        if (!live) {
           uint32_t z[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) z[e] = 0u;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) tmem_st16(tl + b * 128u + c * 16, z);
+          for (int c = 0; c < kC / 16; ++c) tmem_st16(sb + c * 16, z);
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(&ctl->p_full[b]);
           continue;
         }
-        uint32_t sv[128];
+        // keys 0..kmax of this thread's columns are visible
+        const int kmax = row_ok ? row_pos - j * pf::kKeys - half * 64 : -1;
+        uint32_t sv[kC];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          tmem_ld32(tl + b * 128u + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
+        for (int c = 0; c < kC / 32; ++c)
+          tmem_ld32(sb + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
         tmem_wait_ld();
         // scores in the log2 domain; masked keys become -inf.  Eight independent max / sum
         // accumulators keep the dependency chains short.
-        float x[128];
+        float x[kC];
         float mx[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx[i] = -CUDART_INF_F;
-        if (__all_sync(0xffffffffu, kmax >= pf::kKeys - 1)) {  // warp-uniform branch
+        if (__all_sync(0xffffffffu, kmax >= kC - 1)) {  // warp-uniform branch
 #pragma unroll
-          for (int i = 0; i < 128; ++i) {
+          for (int i = 0; i < kC; ++i) {
             x[i] = __uint_as_float(sv[i]) * p.score_log2;
             mx[i & 7] = fmaxf(mx[i & 7], x[i]);
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < 128; ++i) {
+          for (int i = 0; i < kC; ++i) {
             x[i] = (i <= kmax) ? __uint_as_float(sv[i]) * p.score_log2 : -CUDART_INF_F;
             mx[i & 7] = fmaxf(mx[i & 7], x[i]);
           }
         }
-        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        float mt;
+        if (!(ok = exchange(fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))),
+                            false, &mt)))
+          break;
         bool rescale = false;
         float m_new = m_used;
         if (j == 0) {
@@ -387,12 +459,13 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           rescale = true;
         }
         const float alpha = rescale ? fast_exp2(m_used - m_new) : 1.f;
-        // probabilities; bf16 hi halves into columns 0..63 of the buffer, lo into 64..127
+        // probabilities; for every 64 keys, bf16 hi parts into their columns 0..31 and lo
+        // parts into 32..63
         float rsum[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) rsum[i] = 0.f;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < kC / 32; ++c) {
           uint32_t hi[16], lo[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
@@ -402,8 +475,9 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             hi[e] = pack_bf16x2(p0, p1);
             lo[e] = pack_bf16x2(p0 - bf16lo_to_f32(hi[e]), p1 - bf16hi_to_f32(hi[e]));
           }
-          tmem_st16(tl + b * 128u + c * 16, hi);
-          tmem_st16(tl + b * 128u + 64 + c * 16, lo);
+          const uint32_t pc = sb + (c >> 1) * 64 + (c & 1) * 16;
+          tmem_st16(pc, hi);
+          tmem_st16(pc + 32, lo);
         }
         const float rs = ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3])) +
                          ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
@@ -414,39 +488,46 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
               !(ok = wait(&ctl->o_done[(g - 1) % pf::kSBufs], ((g - 1) / pf::kSBufs) & 1u)))
             break;
           tc_fence_after();
-          uint32_t o[128];
+          uint32_t o[kC];
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            tmem_ld32(tl + pf::kOCol + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&o[c * 32]));
+          for (int c = 0; c < kC / 32; ++c)
+            tmem_ld32(tl + pf::kOCol + hc + c * 32,
+                      *reinterpret_cast<uint32_t(*)[32]>(&o[c * 32]));
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 128; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          for (int i = 0; i < kC; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            tmem_st32(tl + pf::kOCol + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&o[c * 32]));
+          for (int c = 0; c < kC / 32; ++c)
+            tmem_st32(tl + pf::kOCol + hc + c * 32,
+                      *reinterpret_cast<uint32_t(*)[32]>(&o[c * 32]));
         }
         tmem_wait_st();
         m_used = m_new;
         tc_fence_before();
         mbar_arrive(&ctl->p_full[b]);
       }
-      // epilogue: O / l
+      // epilogue: the thread's columns of O divided by the row sum (of both halves)
+      if (ok && live) {
+        float lt;
+        ok = exchange(l, true, &lt);
+        l = lt;
+      }
       const uint32_t g_last = tc + I.nkv - 1;
-      if (ok && wait(&ctl->o_done[g_last % pf::kSBufs], (g_last / pf::kSBufs) & 1u)) {
+      if (ok && live && wait(&ctl->o_done[g_last % pf::kSBufs], (g_last / pf::kSBufs) & 1u)) {
         tc_fence_after();
         const float inv = (row_ok && l > 0.f) ? 1.f / l : 0.f;
         const int64_t orow = static_cast<int64_t>(I.t0 + tok) * p.num_q_heads + I.h * G + r % G;
-        uint32_t o[128];
+        uint32_t o[kC];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          tmem_ld32(tl + pf::kOCol + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&o[c * 32]));
+        for (int c = 0; c < kC / 32; ++c)
+          tmem_ld32(tl + pf::kOCol + hc + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&o[c * 32]));
         tmem_wait_ld();
         if (row_ok) {
           if (p.out_bf16) {
-            uint4* dst =
-                reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * 128);
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                                  orow * 128 + hc);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < kC / 8; ++i) {
               uint32_t w[4];
 #pragma unroll
               for (int e = 0; e < 4; ++e)
@@ -455,9 +536,10 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
               dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
             }
           } else {
-            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + orow * 128);
+            float4* dst =
+                reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + orow * 128 + hc);
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
+            for (int i = 0; i < kC / 4; ++i)
               dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv,
                                    __uint_as_float(o[4 * i + 1]) * inv,
                                    __uint_as_float(o[4 * i + 2]) * inv,
@@ -478,7 +560,28 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, pf::kTmemCols);
 }
 
-size_t prefill_smem_bytes() { return pf::kSmem; }
+namespace {
+
+template <bool kSplit>
+cudaError_t launch_prefill_as(const AttnArgs& a, const PrefillParams& p, const CUtensorMap& qmap,
+                              const CUtensorMap& kmap, const CUtensorMap& vmap) {
+  constexpr int kThreads = pf::threads(kSplit), kSmem = pf::smem_bytes(kSplit);
+  LaunchInfo li;
+  cudaError_t e = launch_info(prefill_kernel<kSplit>, kThreads, kSmem, &li);
+  if (e != cudaSuccess) return e;
+  const int64_t upper =
+      static_cast<int64_t>(a.num_kv_heads) *
+      ((static_cast<int64_t>(a.num_q_tokens) * p.group + pf::kRows - 1) / pf::kRows +
+       a.num_seqs);
+  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(upper, li.sms));
+  if (a.pf_before && a.pf_after) cudaEventRecord(a.pf_before, a.stream);
+  prefill_kernel<kSplit>
+      <<<static_cast<unsigned>(grid), kThreads, kSmem, a.stream>>>(qmap, kmap, vmap, p);
+  if (a.pf_before && a.pf_after) cudaEventRecord(a.pf_after, a.stream);
+  return cudaGetLastError();
+}
+
+}  // namespace
 
 cudaError_t launch_prefill(const AttnArgs& a, const int32_t* item_start, WsHeader* hdr,
                            const CUtensorMap& qmap, const CUtensorMap& kmap,
@@ -498,20 +601,12 @@ cudaError_t launch_prefill(const AttnArgs& a, const int32_t* item_start, WsHeade
   p.num_blocks = a.cache.num_blocks;
   p.out_bf16 = a.out_dtype == PA_BF16;
   p.score_log2 = a.scale * 1.4426950408889634f;
-  LaunchInfo li;
-  cudaError_t e = launch_info(prefill_kernel, pf::kThreads, pf::kSmem, &li);
-  if (e != cudaSuccess) return e;
-  const int sms = li.sms;
-  const int G = p.group;
-  const int64_t upper =
-      static_cast<int64_t>(a.num_kv_heads) *
-      ((static_cast<int64_t>(a.num_q_tokens) * G + pf::kRows - 1) / pf::kRows + a.num_seqs);
-  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(upper, sms));
-  if (a.pf_before && a.pf_after) cudaEventRecord(a.pf_before, a.stream);
-  prefill_kernel<<<static_cast<unsigned>(grid), pf::kThreads, pf::kSmem, a.stream>>>(qmap, kmap,
-                                                                                     vmap, p);
-  if (a.pf_before && a.pf_after) cudaEventRecord(a.pf_after, a.stream);
-  return cudaGetLastError();
+  // Runs of at most 64 rows (tokens x group heads: speculative verify) leave at least two of
+  // a tile's four lane quarters empty; splitting each row over two warps then puts a second
+  // warp on the busy quarters' SM sub-partitions.  Fuller tiles gain nothing from the split.
+  if (static_cast<int64_t>(a.max_query_len) * p.group <= 64)
+    return launch_prefill_as<true>(a, p, qmap, kmap, vmap);
+  return launch_prefill_as<false>(a, p, qmap, kmap, vmap);
 }
 
 }  // namespace pa

@@ -95,6 +95,9 @@ def test_multi_query_causal(qlens, ctx, dtype):
     (16, 2, [3, 2, 1], [70, 900, 33]),                # group of 8: 24 rows to the tensor-core
                                                       # tiles, 16 and 8 rows to the split-KV path
     (8, 4, [9, 8, 1], [9, 500, 1200]),                # group of 2: 18 rows vs 16
+    (16, 4, [16, 9, 1], [16, 700, 300]),              # 64 and 36 rows: two lane quarters,
+                                                      # rows split over two warps
+    (16, 4, [20, 3], [900, 50]),                      # 80 rows: whole-row softmax warps
 ])
 @pytest.mark.parametrize("dtype", ["bf16", "fp8_e4m3"])
 def test_multi_query_row_tiles(hq, hkv, qlens, ctx, dtype):
@@ -116,6 +119,21 @@ def test_prefill_chunks_on_tensor_core_tiles(hq, hkv):
     last blocks holding NaN patterns, GQA groups 1, 2, 4, 8, mixed with decode sequences."""
     w = make_workload(PF_CTX + [90, 3000], PF_QL + [1, 1], num_q_heads=hq, num_kv_heads=hkv,
                       head_dim=128, seed=hq * 7 + 1, pool_fill="nan")
+    _check_small(w)
+
+
+@pytest.mark.parametrize("qlens,ctx,dtype", [
+    ([1, 1, 1, 1], [4000, 2000, 513, 100], "bf16"),        # split-KV decode
+    ([1, 1, 1, 1], [4000, 2000, 513, 100], "fp8_e4m3"),
+    ([3, 2], [3000, 700], "bf16"),                          # 16-row split-KV tiles
+    ([100, 40], [2000, 600], "bf16"),                       # tensor-core tiles, whole rows
+    ([5, 16], [1500, 900], "bf16"),                         # tensor-core tiles, split rows
+])
+def test_sharp_scores_rescale_the_running_max(qlens, ctx, dtype):
+    """Unscaled q.k (scale 1: scores of sd ~11 nats) make the running max of a row grow by
+    more than 2^8 as the keys stream in, so the accumulated output is rescaled on the way."""
+    w = make_workload(ctx, qlens, num_q_heads=16, num_kv_heads=4, head_dim=128,
+                      cache_dtype=dtype, seed=sum(ctx) + len(qlens), scale=1.0)
     _check_small(w)
 
 
@@ -142,6 +160,24 @@ def test_prefill_block_permutation_is_bitwise_invariant():
 
 def test_single_sequence_long_context_splits():
     w = make_workload([9000], [1], num_q_heads=8, num_kv_heads=2, head_dim=128, seed=5)
+    _check_small(w)
+
+
+@pytest.mark.parametrize("qlen_long", [1, 3])
+@pytest.mark.parametrize("dtype", ["bf16", "fp8_e4m3"])
+def test_many_sequences_with_splits_past_the_first_thousand(qlen_long, dtype):
+    """1,100 sequences, most of them short; the long ones (split into partitions) sit at the
+    first and last index, at the 32- and 1024-sequence boundaries and in between, so the
+    merge finds each row's sequence in more than one round of its 32-way search."""
+    rng = np.random.default_rng(4100 + qlen_long)
+    n = 1100
+    ctx = rng.integers(1, 48, size=n)
+    qlen = np.ones(n, dtype=np.int64)
+    for s in (0, 31, 32, 517, 1023, 1024, 1099):
+        ctx[s] = 6000 + s
+        qlen[s] = qlen_long
+    w = make_workload(list(ctx), list(qlen), num_q_heads=8, num_kv_heads=2, head_dim=128,
+                      cache_dtype=dtype, seed=41 + qlen_long, pool_fill="nan")
     _check_small(w)
 
 
