@@ -47,6 +47,7 @@ struct DecodeParams {
   const int32_t* qsl;
   int32_t* item_start;
   int32_t* pf_item_start;
+  int32_t* merge_start;    // [S+1] prefix sums of the rows the merge combines
   float* part_lse;
   float* part_o;
   void* out;
@@ -72,6 +73,11 @@ struct DecodeParams {
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Partitions of a decode-path sequence of L keys.
+__device__ __forceinline__ int partitions_of(const DecodeParams& p, int L) {
+  return ceil_div(ceil_div(L, kBlockSize), p.pblk);
+}
+
 // Items of one sequence on the decode path (0 if it belongs to the prefill path or is invalid).
 __device__ __forceinline__ int decode_items_of(const DecodeParams& p, int n, int L, bool* bad) {
   *bad = false;
@@ -87,7 +93,7 @@ __device__ __forceinline__ int decode_items_of(const DecodeParams& p, int n, int
   if (n > p.decode_max_query || n * p.group > p.decode_max_rows) return 0;
   const int tpt = p.rows_per_tile / (p.group * p.heads_per_item);  // query tokens per tile
   const int qtiles = ceil_div(n, tpt);
-  const int nparts = ceil_div(ceil_div(L, kBlockSize), p.pblk);
+  const int nparts = partitions_of(p, L);
   return p.num_kv_heads / p.heads_per_item * qtiles * nparts;
 }
 
@@ -99,68 +105,77 @@ __device__ __forceinline__ int prefill_items_of(const DecodeParams& p, int n, in
   return p.num_kv_heads * ceil_div(n, tpt);
 }
 
-// One CTA: exclusive prefix sums of decode and prefill items over sequences; resets the work
-// counters and flags inconsistent lengths.
+// One CTA: exclusive prefix sums over sequences of decode items, prefill items and merge rows
+// (token x q head rows of decode-path sequences split into two or more partitions); resets the
+// work counters and flags inconsistent lengths.
 __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
   grid_dependency_wait();    // whatever the stream ran before (the step's append) is complete
   grid_launch_dependents();  // the attention kernel may set up its CTAs meanwhile
-  __shared__ int2 warp_sums[32];
-  __shared__ int2 carry_s;
+  constexpr int kN = 3;      // decode items, prefill items, merge rows
+  __shared__ int warp_sums[32][kN];
+  __shared__ int carry_s[kN];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) carry_s = make_int2(0, 0);
+  if (tid < kN) carry_s[tid] = 0;
   __syncthreads();
   for (int base = 0; base < p.num_seqs; base += 1024) {
     const int s = base + tid;
-    int2 cnt = make_int2(0, 0);
+    int cnt[kN] = {0, 0, 0};
     if (s < p.num_seqs) {
       const int n = p.qsl[s + 1] - p.qsl[s];
       const int L = p.context_lens[s];
       bool bad;
-      cnt.x = decode_items_of(p, n, L, &bad);
+      cnt[0] = decode_items_of(p, n, L, &bad);
       if (bad) set_error(&p.hdr->error, PA_DEVERR_LENGTHS);
-      cnt.y = prefill_items_of(p, n, L);
+      cnt[1] = prefill_items_of(p, n, L);
+      cnt[2] = (cnt[0] > 0 && partitions_of(p, L) > 1) ? n * p.num_q_heads : 0;
     }
-    int2 x = cnt;  // inclusive warp scan of both counts
+    int x[kN];  // inclusive warp scans
+#pragma unroll
+    for (int k = 0; k < kN; ++k) x[k] = cnt[k];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int yx = __shfl_up_sync(0xffffffffu, x.x, o);
-      const int yy = __shfl_up_sync(0xffffffffu, x.y, o);
-      if (lane >= o) {
-        x.x += yx;
-        x.y += yy;
+#pragma unroll
+      for (int k = 0; k < kN; ++k) {
+        const int y = __shfl_up_sync(0xffffffffu, x[k], o);
+        if (lane >= o) x[k] += y;
       }
     }
-    if (lane == 31) warp_sums[warp] = x;
+    if (lane == 31)
+#pragma unroll
+      for (int k = 0; k < kN; ++k) warp_sums[warp][k] = x[k];
     __syncthreads();
     if (warp == 0) {
-      int2 w = warp_sums[lane];
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int yx = __shfl_up_sync(0xffffffffu, w.x, o);
-        const int yy = __shfl_up_sync(0xffffffffu, w.y, o);
-        if (lane >= o) {
-          w.x += yx;
-          w.y += yy;
+      for (int k = 0; k < kN; ++k) {
+        int w = warp_sums[lane][k];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, w, o);
+          if (lane >= o) w += y;
         }
+        warp_sums[lane][k] = w;  // inclusive over warps
       }
-      warp_sums[lane] = w;  // inclusive over warps
     }
     __syncthreads();
-    const int2 carry = carry_s;
-    const int2 before = warp ? warp_sums[warp - 1] : make_int2(0, 0);
-    const int2 excl = make_int2(carry.x + before.x + x.x - cnt.x,
-                                carry.y + before.y + x.y - cnt.y);
+    int excl[kN];
+#pragma unroll
+    for (int k = 0; k < kN; ++k)
+      excl[k] = carry_s[k] + (warp ? warp_sums[warp - 1][k] : 0) + x[k] - cnt[k];
     if (s < p.num_seqs) {
-      p.item_start[s] = excl.x;
-      p.pf_item_start[s] = excl.y;
+      p.item_start[s] = excl[0];
+      p.pf_item_start[s] = excl[1];
+      p.merge_start[s] = excl[2];
     }
     __syncthreads();
-    if (tid == 1023) carry_s = make_int2(excl.x + cnt.x, excl.y + cnt.y);
+    if (tid == 1023)
+#pragma unroll
+      for (int k = 0; k < kN; ++k) carry_s[k] = excl[k] + cnt[k];
     __syncthreads();
   }
   if (tid == 0) {
-    p.item_start[p.num_seqs] = carry_s.x;
-    p.pf_item_start[p.num_seqs] = carry_s.y;
+    p.item_start[p.num_seqs] = carry_s[0];
+    p.pf_item_start[p.num_seqs] = carry_s[1];
+    p.merge_start[p.num_seqs] = carry_s[2];
     p.hdr->decode_counter = 0;
     p.hdr->prefill_counter = 0;
   }
@@ -704,36 +719,10 @@ __device__ __forceinline__ void load_batch8<2>(const float* const (&src)[8], flo
         "l"(src[6]), "l"(src[7]));
 }
 
-// One warp per (token, q head) row of a sequence that was split into several partitions.
+// Combines the partials of one row: out = sum_j 2^(lse_j - M) o_j / sum_j 2^(lse_j - M).
 template <int D>
-// (At least 2 CTAs per SM, i.e. up to 128 registers a thread: room for the sixteen loads in
-// flight, which a full-occupancy register budget of 32 would serialise.)
-__global__ void __launch_bounds__(256, 2)
-    merge_kernel(const DecodeParams p, int32_t num_tokens) {
-  grid_dependency_wait();  // the attention kernel's partials are complete
-  const int lane = threadIdx.x & 31;
-  const int64_t rid = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  if (rid >= static_cast<int64_t>(num_tokens) * p.num_q_heads) return;
-  const int t = static_cast<int>(rid / p.num_q_heads);
-  // sequence of token t, the largest s with qsl[s] <= t (qsl is non-decreasing, qsl[0] = 0):
-  // a 32-way search by the warp, one coalesced load per round
-  int lo = 0, span = p.num_seqs;
-  while (span > 32) {
-    const int step = (span + 31) >> 5;
-    const int idx = lo + lane * step;
-    const int start = idx < lo + span ? p.qsl[idx] : INT_MAX;
-    const int last = 31 - __clz(__ballot_sync(0xffffffffu, start <= t));
-    lo += last * step;
-    span = min(step, span - last * step);
-  }
-  const int start = lane < span ? p.qsl[lo + lane] : INT_MAX;
-  const int s = lo + 31 - __clz(__ballot_sync(0xffffffffu, start <= t));
-  const int n = p.qsl[s + 1] - p.qsl[s];
-  const int L = p.context_lens[s];
-  bool bad;
-  if (decode_items_of(p, n, L, &bad) == 0) return;  // prefill path, invalid, or empty
-  const int nparts = ceil_div(ceil_div(L, kBlockSize), p.pblk);
-  if (nparts <= 1) return;
+__device__ __forceinline__ void merge_row(const DecodeParams& p, int64_t rid, int nparts,
+                                          int lane) {
   const float* lse = p.part_lse + rid * p.pmax;
   float M = -CUDART_INF_F;
   for (int i = lane; i < nparts; i += 32) M = fmaxf(M, lse[i]);
@@ -785,6 +774,39 @@ __global__ void __launch_bounds__(256, 2)
   }
 }
 
+// One warp per row (token, q head) of a sequence that was split into several partitions: the
+// plan lists those rows (merge_start), and a grid of at most one resident wave strides over
+// them.
+template <int D>
+// (At least 2 CTAs per SM, i.e. up to 128 registers a thread: room for the sixteen loads in
+// flight, which a full-occupancy register budget of 32 would serialise.)
+__global__ void __launch_bounds__(256, 2) merge_kernel(const DecodeParams p) {
+  grid_dependency_wait();  // the attention kernel's partials (and the plan) are complete
+  const int lane = threadIdx.x & 31;
+  const int total = p.merge_start[p.num_seqs];
+  const int stride = gridDim.x * 8;
+#pragma unroll 1
+  for (int c = blockIdx.x * 8 + (threadIdx.x >> 5); c < total; c += stride) {
+    // sequence of merge row c, the largest s with merge_start[s] <= c (merge_start is
+    // non-decreasing from 0; a sequence without rows has an empty range): a 32-way search by
+    // the warp, one coalesced load per round
+    int lo = 0, span = p.num_seqs;
+    while (span > 32) {
+      const int step = (span + 31) >> 5;
+      const int idx = lo + lane * step;
+      const int start = idx < lo + span ? p.merge_start[idx] : INT_MAX;
+      const int last = 31 - __clz(__ballot_sync(0xffffffffu, start <= c));
+      lo += last * step;
+      span = min(step, span - last * step);
+    }
+    const int start = lane < span ? p.merge_start[lo + lane] : INT_MAX;
+    const int s = lo + 31 - __clz(__ballot_sync(0xffffffffu, start <= c));
+    const int local = c - p.merge_start[s];
+    const int64_t rid = static_cast<int64_t>(p.qsl[s]) * p.num_q_heads + local;
+    merge_row<D>(p, rid, partitions_of(p, p.context_lens[s]), lane);
+  }
+}
+
 template <int D, bool kFp8, int NST, int RT, int HPI = 1>
 static cudaError_t run_decode(const AttnArgs& a, const WsLayout& ws, const DecodeParams& p,
                               const CUtensorMap& kmap, const CUtensorMap& vmap,
@@ -806,11 +828,14 @@ static cudaError_t run_decode(const AttnArgs& a, const WsLayout& ws, const Decod
   if (after) cudaEventRecord(after, a.stream);
   if (e != cudaSuccess) return e;
   if (ws.pmax > 1) {
+    // at most one resident wave of 8-warp CTAs; the merge rows are fewer than all rows
+    LaunchInfo mi;
+    if ((e = launch_info(merge_kernel<D>, 256, 0, &mi)) != cudaSuccess) return e;
     const int64_t rows = static_cast<int64_t>(a.num_q_tokens) * a.num_q_heads;
-    const int64_t blocks = (rows + 7) / 8;
+    const int64_t blocks = std::min<int64_t>((rows + 7) / 8, int64_t(mi.sms) * mi.per_sm);
     if (blocks > 0)
       e = launch_dependent(merge_kernel<D>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
-                           a.stream, p, a.num_q_tokens);
+                           a.stream, p);
   }
   return e;
 }
@@ -843,6 +868,7 @@ cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const CUtens
   p.qsl = a.query_start_loc;
   p.item_start = reinterpret_cast<int32_t*>(wsb + ws.item_start);
   p.pf_item_start = reinterpret_cast<int32_t*>(wsb + ws.pf_item_start);
+  p.merge_start = reinterpret_cast<int32_t*>(wsb + ws.merge_start);
   p.part_lse = reinterpret_cast<float*>(wsb + ws.part_lse);
   p.part_o = reinterpret_cast<float*>(wsb + ws.part_o);
   p.out = a.out;

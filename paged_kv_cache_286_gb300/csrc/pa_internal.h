@@ -59,6 +59,8 @@ struct AttnArgs {
 struct WsLayout {
   size_t item_start;  // int32 [num_seqs + 1], decode work-item prefix sums
   size_t pf_item_start;  // int32 [num_seqs + 1], prefill work-item prefix sums
+  size_t merge_start;  // int32 [num_seqs + 1], prefix sums of the rows (token x q head) that
+                       // the merge combines: those of split-KV sequences with 2+ partitions
   size_t part_lse;    // float [num_q_tokens][num_q_heads][pmax], log2-domain log-sum-exp
   size_t part_o;      // float [num_q_tokens][num_q_heads][pmax][head_dim], normalised partials
   size_t total;
