@@ -108,8 +108,13 @@ __device__ __forceinline__ int prefill_items_of(const DecodeParams& p, int n, in
 // One CTA: exclusive prefix sums over sequences of decode items, prefill items and merge rows
 // (token x q head rows of decode-path sequences split into two or more partitions); resets the
 // work counters and flags inconsistent lengths.
+//
+// It reads only the step's metadata (query_start_loc, context_lens), never the pools, so it runs
+// beside the step's append and waits for the append only before it exits; the attention kernel,
+// which waits for the plan, therefore still sees every appended key.  It starts early only after
+// the append kernel, which itself waited for all earlier work on the stream before letting it
+// launch, so no earlier step's kernel still reads the workspace it writes.
 __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
-  grid_dependency_wait();    // whatever the stream ran before (the step's append) is complete
   grid_launch_dependents();  // the attention kernel may set up its CTAs meanwhile
   constexpr int kN = 3;      // decode items, prefill items, merge rows
   __shared__ int warp_sums[32][kN];
@@ -179,6 +184,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
     p.hdr->decode_counter = 0;
     p.hdr->prefill_counter = 0;
   }
+  grid_dependency_wait();  // the plan completes only after the stream's earlier work (the append)
 }
 
 template <int D, bool kFp8, int HPI = 1>
