@@ -309,24 +309,32 @@ def prefill_flops(w) -> int:
     return 4 * w.head_dim * w.num_q_heads * total
 
 
-def decode_src_sha() -> str:
+def src_sha(files=None) -> str:
+    """sha256 (first 16 hex digits) over names and contents of kernel source files under csrc/:
+    the named ones in the given order, or all of them sorted by name."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_286_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in (files if files is not None else sorted(os.listdir(csrc))):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
+def decode_src_sha() -> str:
+    """Hash of all kernel sources (the label the profile summaries carry)."""
+    return src_sha()
+
+
 def traffic_from_profiles(config_id: int):
-    """DRAM bytes per launch of the attention kernel from a committed ncu summary, if it was
-    taken from the current kernel sources (else None)."""
+    """DRAM bytes per launch of the step's dominant kernel from a committed ncu summary, if the
+    source files that define that kernel (its entry's src_files) are unchanged since the
+    counters were taken (else None)."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             j = json.load(f)
         e = j.get(f"cfg{config_id}")
-        if e and e.get("src_sha") == decode_src_sha():
+        if e and e.get("src_sha") == src_sha(e.get("src_files")):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass
