@@ -21,7 +21,8 @@ def lib():
 
 
 def header_functions():
-    text = open(os.path.join(ROOT, "include", "pa.h")).read()
+    with open(os.path.join(ROOT, "include", "pa.h")) as f:
+        text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(pa_[a-z_0-9]+)\s*\(", text)))
 
@@ -44,7 +45,8 @@ def test_library_exports_every_declared_function(lib):
 
 
 def test_block_manager_header_is_exported(lib):
-    text = open(os.path.join(ROOT, "include", "pa_block_manager.h")).read()
+    with open(os.path.join(ROOT, "include", "pa_block_manager.h")) as f:
+        text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     names = sorted(set(re.findall(r"\b(pa_bm_[a-z_0-9]+)\s*\(", text)))
     from paged_kv_cache_286_gb300 import _lib

@@ -35,7 +35,7 @@ def _worker(rank, world, port, results):
 @pytest.mark.timeout(120)
 def test_two_replicas_report_the_slowest_rank():
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:  # no fork of this multi-threaded process
         results = m.dict()
         mp.spawn(_worker, args=(2, port, results), nprocs=2, join=True)
         assert dict(results) == {0: 2.0, 1: 2.0}
