@@ -110,6 +110,9 @@ def test_append_rejects_null_and_negative(lib):
     assert lib.pa_cache_append(None, FAKE, FAKE, 4, FAKE, FAKE, ctypes.byref(d), FAKE, None) == 1
     assert lib.pa_cache_append(FAKE, FAKE, FAKE, 4, FAKE, FAKE, None, FAKE, None) == 1
     assert lib.pa_cache_append(FAKE, FAKE, FAKE, 0, FAKE, FAKE, ctypes.byref(d), None, None) == 1
+    misaligned = ctypes.c_void_p(0x100008)  # 8 bytes past a 16-byte boundary
+    assert lib.pa_cache_append(misaligned, FAKE, FAKE, 4, FAKE, FAKE, ctypes.byref(d), FAKE,
+                               None) == 1
     # zero tokens with valid arguments is a no-op that touches nothing
     assert lib.pa_cache_append(FAKE, FAKE, FAKE, 0, FAKE, FAKE, ctypes.byref(d), FAKE, None) == 0
 
@@ -139,6 +142,11 @@ def _attn(lib, **kw):
     (dict(ws=ctypes.c_void_p(0x100010)), 1),  # workspace not 256-byte aligned
     (dict(S=-1), 1),
     (dict(desc=_desc(cache_dtype=1, head_dim=64)), 2),   # fp8 attention needs head_dim 128
+    (dict(q=ctypes.c_void_p(0x100002)), 1),  # q not 16-byte aligned
+    (dict(maxq=0), 1),                       # host hints must be positive
+    (dict(maxb=0), 1),
+    (dict(hkv=0), 1),                        # no kv heads
+    (dict(desc=_desc(num_blocks=1 << 26)), 1),  # 2^32 pool rows: beyond the 32-bit row index
 ])
 def test_attention_rejects_bad_arguments(lib, kw, status):
     assert _attn(lib, **kw) == status
