@@ -75,7 +75,8 @@ typedef enum {
 typedef enum { PA_BF16 = 0, PA_FP8_E4M3 = 1, PA_FP32 = 2 } pa_dtype;
 
 /* Geometry of one pool (both k_cache and v_cache).  Supported: block_size 16; head_dim 64 or
- * 128 for bf16, 128 for PA_FP8_E4M3.  k_scale / v_scale are used only for PA_FP8_E4M3. */
+ * 128 for bf16, 128 for PA_FP8_E4M3; num_blocks * num_kv_heads * block_size (the pool's rows)
+ * at most 2^31 - 1.  k_scale / v_scale are used only for PA_FP8_E4M3. */
 typedef struct {
   int32_t num_blocks;
   int32_t block_size;
@@ -174,7 +175,9 @@ pa_status pa_attention(const void* q, int32_t num_q_tokens, const void* k_cache,
  * PA_ERR_INVALID_ARG and a message; use pa_attention with a workspace for larger steps.
  *   Arguments are those of pa_attention without workspace/workspace_bytes, plus
  *   error_word    optional DEVICE pointer (may be NULL) that receives, asynchronously on
- *                 `stream`, this call's PA_DEVERR_* bits.
+ *                 `stream`, this call's PA_DEVERR_* bits (0 for a step with nothing to do).  It
+ *                 is written only when the call returns PA_OK; a call rejected on the host
+ *                 changes neither *error_word nor the scratch array.
  * The first call on a device looks up the scratch array's device address (once per device, with
  * that device current); make that first call before any stream capture.  Every call shares the
  * one array and overwrites it, starting from a cleared header: calls whose GPU work overlaps

@@ -115,9 +115,12 @@ pa_status check_cache_desc(const pa_cache_desc* c, bool for_attention) {
       return fail(PA_ERR_UNSUPPORTED,
                   "attention over head_dim %d with this cache dtype is not built", c->head_dim);
   }
-  const double rows = double(c->num_blocks) * c->num_kv_heads * c->block_size;
-  if (rows >= 4294967296.0 || rows * c->head_dim >= 9.2e18)
-    return fail(PA_ERR_INVALID_ARG, "pool too large");
+  // The kernels address a pool row (block, kv head, slot) with a signed 32-bit TMA coordinate.
+  const int64_t rows = int64_t(c->num_blocks) * c->num_kv_heads * c->block_size;
+  if (rows > int64_t(INT32_MAX))
+    return fail(PA_ERR_INVALID_ARG,
+                "pool too large: %lld rows of (block, kv head, slot), at most 2^31 - 1",
+                static_cast<long long>(rows));
   return PA_OK;
 }
 
@@ -233,6 +236,46 @@ cudaError_t side_stream(SideStream* out) {
 // pa_last_error_string.
 void set_last_error(const char* msg) { g_last_error = msg; }
 
+pa_status check_attention_args(const void* q, int32_t num_q_tokens, const void* k_cache,
+                               const void* v_cache, const pa_cache_desc* cache,
+                               const int32_t* block_tables, int32_t max_blocks_per_seq,
+                               const int32_t* context_lens, const int32_t* query_start_loc,
+                               int32_t num_seqs, int32_t max_context_len, int32_t max_query_len,
+                               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                               float scale, const void* out, int32_t out_dtype, bool* nothing) {
+  g_last_error.clear();
+  *nothing = false;
+  if (num_seqs < 0 || num_q_tokens < 0) return fail(PA_ERR_INVALID_ARG, "negative size");
+  pa_status st = check_cache_desc(cache, true);
+  if (st != PA_OK) return st;
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+    return fail(PA_ERR_INVALID_ARG, "non-positive head count or head_dim");
+  if (num_q_heads % num_kv_heads != 0)
+    return fail(PA_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d",
+                num_q_heads, num_kv_heads);
+  if (num_q_heads / num_kv_heads > kDecodeMaxGroup)
+    return fail(PA_ERR_UNSUPPORTED, "GQA group of %d q heads per kv head is not built (<= 16)",
+                num_q_heads / num_kv_heads);
+  if (head_dim != cache->head_dim || num_kv_heads != cache->num_kv_heads)
+    return fail(PA_ERR_INVALID_ARG, "head_dim / num_kv_heads disagree with the cache descriptor");
+  if (out_dtype != PA_FP32 && out_dtype != PA_BF16)
+    return fail(PA_ERR_UNSUPPORTED, "out_dtype %d is not built", out_dtype);
+  if (!(std::isfinite(scale))) return fail(PA_ERR_INVALID_ARG, "scale is not finite");
+  if (num_seqs == 0 || num_q_tokens == 0) {
+    *nothing = true;
+    return PA_OK;
+  }
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start_loc || !out)
+    return fail(PA_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (max_blocks_per_seq <= 0 || max_context_len <= 0 || max_query_len <= 0)
+    return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq, max_context_len and max_query_len must "
+                                    "be positive");
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(query_start_loc, 4))
+    return fail(PA_ERR_INVALID_ARG, "misaligned pointer (q, out and caches need 16 bytes)");
+  return PA_OK;
+}
+
 }  // namespace pa
 
 extern "C" {
@@ -333,35 +376,16 @@ pa_status pa_attention(const void* q, int32_t num_q_tokens, const void* k_cache,
                        int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, float scale,
                        void* out, int32_t out_dtype, void* workspace, size_t workspace_bytes,
                        cudaStream_t stream) {
-  g_last_error.clear();
-  if (num_seqs < 0 || num_q_tokens < 0) return fail(PA_ERR_INVALID_ARG, "negative size");
-  pa_status st = check_cache_desc(cache, true);
+  bool nothing = false;
+  pa_status st = pa::check_attention_args(
+      q, num_q_tokens, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, context_lens,
+      query_start_loc, num_seqs, max_context_len, max_query_len, num_q_heads, num_kv_heads,
+      head_dim, scale, out, out_dtype, &nothing);
   if (st != PA_OK) return st;
-  if (num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0)
-    return fail(PA_ERR_INVALID_ARG, "non-positive head count or head_dim");
-  if (num_q_heads % num_kv_heads != 0)
-    return fail(PA_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d",
-                num_q_heads, num_kv_heads);
-  if (num_q_heads / num_kv_heads > pa::kDecodeMaxGroup)
-    return fail(PA_ERR_UNSUPPORTED, "GQA group of %d q heads per kv head is not built (<= 16)",
-                num_q_heads / num_kv_heads);
-  if (head_dim != cache->head_dim || num_kv_heads != cache->num_kv_heads)
-    return fail(PA_ERR_INVALID_ARG, "head_dim / num_kv_heads disagree with the cache descriptor");
-  if (out_dtype != PA_FP32 && out_dtype != PA_BF16)
-    return fail(PA_ERR_UNSUPPORTED, "out_dtype %d is not built", out_dtype);
-  if (!(std::isfinite(scale))) return fail(PA_ERR_INVALID_ARG, "scale is not finite");
   if (!workspace) return fail(PA_ERR_INVALID_ARG, "workspace is NULL");
-  if (num_seqs == 0 || num_q_tokens == 0) return PA_OK;
-  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start_loc || !out)
-    return fail(PA_ERR_INVALID_ARG, "NULL tensor pointer");
-  if (max_blocks_per_seq <= 0 || max_context_len <= 0 || max_query_len <= 0)
-    return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq, max_context_len and max_query_len must "
-                                    "be positive");
-  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
-      !aligned(workspace, 256) || !aligned(block_tables, 4) || !aligned(context_lens, 4) ||
-      !aligned(query_start_loc, 4))
-    return fail(PA_ERR_INVALID_ARG, "misaligned pointer (q, out and caches need 16 bytes, the "
-                                    "workspace 256)");
+  if (nothing) return PA_OK;
+  if (!aligned(workspace, 256))
+    return fail(PA_ERR_INVALID_ARG, "misaligned pointer (the workspace needs 256 bytes)");
   const pa::WsLayout ws = pa::workspace_layout(num_seqs, num_q_tokens, num_q_heads, num_kv_heads,
                                                head_dim, max_context_len, max_query_len);
   if (workspace_bytes < ws.total)

@@ -109,13 +109,13 @@ __device__ __forceinline__ int prefill_items_of(const DecodeParams& p, int n, in
 // (token x q head rows of decode-path sequences split into two or more partitions); resets the
 // work counters and flags inconsistent lengths.
 //
-// It reads only the step's metadata (query_start_loc, context_lens), never the pools, so it runs
-// beside the step's append and waits for the append only before it exits; the attention kernel,
-// which waits for the plan, therefore still sees every appended key.  It starts early only after
-// the append kernel, which itself waited for all earlier work on the stream before letting it
-// launch, so no earlier step's kernel still reads the workspace it writes.
+// It is launched early (programmatic dependent launch) and lets the attention kernel set up its
+// CTAs meanwhile, but it waits for all earlier work of the stream before it reads anything: the
+// caller may have written query_start_loc or context_lens with any kernel just before, and an
+// earlier step may still be reading the workspace the plan overwrites.
 __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
   grid_launch_dependents();  // the attention kernel may set up its CTAs meanwhile
+  grid_dependency_wait();    // every earlier kernel of the stream is complete and visible
   constexpr int kN = 3;      // decode items, prefill items, merge rows
   __shared__ int warp_sums[32][kN];
   __shared__ int carry_s[kN];
@@ -184,7 +184,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
     p.hdr->decode_counter = 0;
     p.hdr->prefill_counter = 0;
   }
-  grid_dependency_wait();  // the plan completes only after the stream's earlier work (the append)
 }
 
 template <int D, bool kFp8, int HPI = 1>

@@ -53,6 +53,23 @@ extern "C" pa_status pa_attention_noalloc(
     int32_t max_context_len, int32_t max_query_len, int32_t num_q_heads, int32_t num_kv_heads,
     int32_t head_dim, float scale, void* out, int32_t out_dtype, uint32_t* error_word,
     cudaStream_t stream) {
+  // Every host-side check runs before the shared scratch is touched, so a rejected call leaves
+  // both the scratch and *error_word as they were.
+  bool nothing = false;
+  pa_status st = pa::check_attention_args(
+      q, num_q_tokens, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, context_lens,
+      query_start_loc, num_seqs, max_context_len, max_query_len, num_q_heads, num_kv_heads,
+      head_dim, scale, out, out_dtype, &nothing);
+  if (st != PA_OK) return st;
+  if (nothing) {
+    if (!error_word) return PA_OK;
+    const cudaError_t e = cudaMemsetAsync(error_word, 0, sizeof(uint32_t), stream);
+    if (e == cudaSuccess) return PA_OK;
+    char msg[256];
+    snprintf(msg, sizeof(msg), "pa_attention_noalloc: %s", cudaGetErrorString(e));
+    pa::set_last_error(msg);
+    return PA_ERR_CUDA;
+  }
   const size_t need = pa_attention_workspace_size(num_seqs, num_q_tokens, num_q_heads,
                                                   num_kv_heads, head_dim, pa::kBlockSize,
                                                   max_context_len, max_query_len);
@@ -81,7 +98,7 @@ extern "C" pa_status pa_attention_noalloc(
     pa::set_last_error(msg);
     return PA_ERR_CUDA;
   }
-  const pa_status st = pa_attention(q, num_q_tokens, k_cache, v_cache, cache, block_tables,
+  st = pa_attention(q, num_q_tokens, k_cache, v_cache, cache, block_tables,
                                     max_blocks_per_seq, context_lens, query_start_loc, num_seqs,
                                     max_context_len, max_query_len, num_q_heads, num_kv_heads,
                                     head_dim, scale, out, out_dtype, scratch,

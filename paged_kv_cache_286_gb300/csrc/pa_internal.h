@@ -78,6 +78,16 @@ cudaError_t launch_cache_append(const void* k, const void* v, const int64_t* slo
 
 void set_last_error(const char* msg);
 
+// Host checks of pa_attention's arguments other than the workspace (clears, then sets, the
+// calling thread's last error).  *nothing is set when the step has no query token or sequence.
+pa_status check_attention_args(const void* q, int32_t num_q_tokens, const void* k_cache,
+                               const void* v_cache, const pa_cache_desc* cache,
+                               const int32_t* block_tables, int32_t max_blocks_per_seq,
+                               const int32_t* context_lens, const int32_t* query_start_loc,
+                               int32_t num_seqs, int32_t max_context_len, int32_t max_query_len,
+                               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                               float scale, const void* out, int32_t out_dtype, bool* nothing);
+
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const pa_cache_desc& c,
                                const int32_t* pairs, int32_t num_pairs, uint32_t* err,
                                cudaStream_t stream);

@@ -147,6 +147,7 @@ def _attn(lib, **kw):
     (dict(maxb=0), 1),
     (dict(hkv=0), 1),                        # no kv heads
     (dict(desc=_desc(num_blocks=1 << 26)), 1),  # 2^32 pool rows: beyond the 32-bit row index
+    (dict(desc=_desc(num_blocks=1 << 25)), 1),  # 2^31 pool rows: one past the signed index
 ])
 def test_attention_rejects_bad_arguments(lib, kw, status):
     assert _attn(lib, **kw) == status
