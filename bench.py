@@ -3,8 +3,9 @@
 
 A step is the whole hot path over one batch: pa_cache_append of the step's new tokens through
 the slot mapping, then pa_attention of every query token over its sequence's paged K/V.  The
-default workload is the 7B-class MHA decode step (32 heads x 128, block 16, 64 sequences with
-contexts uniform in [512, 4096], bf16 K/V); --config picks another of the five named workloads.
+headline workload is the 7B-class MHA decode step (32 heads x 128, block 16, 64 sequences
+with contexts uniform in [512, 4096], bf16 K/V); by default every named workload (1-6) is also
+timed the same way and reported under `per_config`, and --config C times workload C alone.
 
 Prints one JSON line.  `value` is achieved HBM GB/s of the step (algorithmic bytes: every unique
 K/V block touched once, q read, out written, metadata, plus the append's reads and writes,
@@ -14,7 +15,8 @@ step's library calls (every kernel runs every replay; the eager per-step time is
 beside it as `eager_ms_per_step`).  `e2e` is the same metric through the public API with the
 step's inputs copied from pinned host memory and the output copied back inside the timed
 region.  `roofline` reports the main attention kernel alone, timed with CUDA events recorded
-around it by the library.  `cpu_baseline` times the fp64 oracle on a bounded sample.
+around it by the library.  `cpu_baseline` times the fp64 oracle on bounded samples of the
+workload, on every host core (one process each) and on one core.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference]
 
@@ -52,7 +54,9 @@ def parse_args(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5, 6])
+    ap.add_argument("--config", type=int, default=0, choices=[0, 1, 2, 3, 4, 5, 6],
+                    help="one named workload only (0: the 7B-class MHA decode headline plus "
+                         "every named workload under per_config)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seqs", type=int, default=0,
                     help="keep only the first N sequences of the workload (small profiling "
@@ -344,77 +348,146 @@ def traffic_from_profiles(config_id: int):
 # ---------------------------------------------------------------------------------------------
 # the oracle on the host cores (CPU baseline and reference arm)
 # ---------------------------------------------------------------------------------------------
-def _oracle_sample_worker(args):
-    """Runs in a spawned process with one BLAS thread: the oracle's whole step (append of the
-    prior context and the new tokens, then attention) on the first `k` sequences."""
-    config_id, k = args
-    sys.path.insert(0, ROOT)
-    from oracle import run_step
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part", "processor\t: arm")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def _sub_workload(config_id: int, first: int, k: int):
+    """k sequences of a named workload (its length recipe, from sequence `first` on, wrapping
+    around), drawn with a seed of their own: a bounded sample of the same workload."""
     from synthetic.workloads import config_lengths, make_workload
     ctx, ql, kw = config_lengths(config_id)
-    w = make_workload(ctx[:k], ql[:k], seed=1000 + config_id, name=f"cfg{config_id}-sample",
-                      **kw)
+    S = len(ctx)
+    idx = [(first + i) % S for i in range(k)]
+    kw = dict(kw)
+    kw.pop("num_blocks", None)
+    return make_workload([ctx[i] for i in idx], [ql[i] for i in idx],
+                         seed=1000 + config_id + 7919 * first,
+                         name=f"cfg{config_id}-sample{first}+{k}", **kw)
+
+
+_SHARDS = {}
+
+
+def _shard_run(args):
+    """In a spawned oracle worker: the oracle's whole step (set-up append, step append,
+    attention) on shard `shard` of k sequences; returns (seconds, bytes, attended tokens)."""
+    config_id, shard, k = args
+    if ROOT not in sys.path:
+        sys.path.insert(0, ROOT)
+    from oracle import run_step
+    key = (config_id, shard, k)
+    if key not in _SHARDS:
+        _SHARDS.clear()
+        _SHARDS[key] = _sub_workload(config_id, shard * k, k)
+    w = _SHARDS[key]
     t0 = time.perf_counter()
     run_step(w)
     dt = time.perf_counter() - t0
-    return dt, w.algorithmic_bytes() + w.append_bytes(), w.attended_tokens(), k
+    return dt, w.algorithmic_bytes() + w.append_bytes(), w.attended_tokens()
 
 
-def oracle_sample(config_id: int, seconds: float):
-    """Time the oracle on growing sub-batches of the workload until one takes >= `seconds`/4,
-    then report the largest; returns dict(value GB/s, tokens/s, seqs, seconds)."""
-    from synthetic.workloads import config_lengths
-    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        os.environ[var] = "1"
-    ctx, _, _ = config_lengths(config_id)
-    S = len(ctx)
-    ctxmp = mp.get_context("spawn")
-    k, best = 1, None
-    with ctxmp.Pool(1) as pool:
+class OracleRunner:
+    """The fp64 oracle, as it stands, on `cores` host processes (spawned, one BLAS thread
+    each); a step is one shard of k sequences per process, timed as the wall time of all."""
+
+    def __init__(self, config_id: int, cores: int):
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[var] = "1"
+        self.config_id, self.cores = config_id, cores
+        self.pool = mp.get_context("spawn").Pool(cores)
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+    def one_core(self, seconds: float):
+        """Grow one process's shard until it takes >= seconds/4; (seconds, bytes, tokens, k)."""
+        from synthetic.workloads import config_lengths
+        S = len(config_lengths(self.config_id)[0])
+        k = 1
         while True:
-            dt, nbytes, toks, k = pool.apply(_oracle_sample_worker, ((config_id, k),))
-            best = (dt, nbytes, toks, k)
+            dt, nbytes, toks = self.pool.apply(_shard_run, ((self.config_id, 0, k),))
             if dt >= seconds / 4 or k >= S:
-                break
+                return dt, nbytes, toks, k
             k = min(S, max(k + 1, int(k * min(4.0, (seconds / 4) / max(dt, 1e-3)))))
-    dt, nbytes, toks, k = best
-    return {"value": nbytes / dt / 1e9, "tokens_per_s": toks / dt, "seqs": k, "of_seqs": S,
-            "seconds": dt}
+
+    def step(self, k: int):
+        """All processes at once, shard i each; returns (wall seconds, bytes, tokens)."""
+        t0 = time.perf_counter()
+        res = self.pool.map(_shard_run, [(self.config_id, i, k) for i in range(self.cores)],
+                            chunksize=1)
+        wall = time.perf_counter() - t0
+        return wall, sum(r[1] for r in res), sum(r[2] for r in res)
+
+
+def cpu_baseline(config_id: int, seconds: float):
+    """One-core and all-core throughput of the oracle on bounded samples of the workload."""
+    cores = host_cores()
+    run = OracleRunner(config_id, cores)
+    try:
+        dt1, b1, t1, k = run.one_core(seconds)
+        run.step(k)                       # every process builds its shard
+        wall, nbytes, toks = run.step(k)
+    finally:
+        run.close()
+    return {"value": nbytes / wall / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{cores} processes (one per host core, one BLAS thread each), each the "
+                      f"fp64 oracle step (set-up append, step append, attention) on its own "
+                      f"{k} sequences of the workload's recipe; wall time {wall:.1f} s",
+            "tokens_per_s": toks / wall, "cpu": cpu_model(),
+            "value_1core": b1 / dt1 / 1e9, "tokens_per_s_1core": t1 / dt1,
+            "sample_1core": f"{k} sequences in one process, {dt1:.1f} s"}
 
 
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    from synthetic.workloads import CONFIG_NAMES, config_lengths
-    ctx, _, _ = config_lengths(args.config)
+    from synthetic.workloads import CONFIG_NAMES
+    cores = host_cores()
     budget = 150.0 / max(1, args.steps + args.warmup)   # whole run within a few minutes
-    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        os.environ[var] = "1"
-    ctxmp = mp.get_context("spawn")
-    with ctxmp.Pool(1) as pool:
-        # size the per-step sample from a one-sequence calibration
-        dt1, _, _, _ = pool.apply(_oracle_sample_worker, ((args.config, 1),))
-        k = max(1, min(len(ctx), int(budget / max(dt1, 1e-3))))
+    run = OracleRunner(args.config, cores)
+    try:
+        dt1 = run.pool.apply(_shard_run, ((args.config, 0, 1),))[0]
+        k = max(1, int(0.8 * budget / max(dt1, 1e-3)))
         times, nbytes, toks = [], 0, 0
         for i in range(args.warmup + args.steps):
-            dt, nb, tk, _ = pool.apply(_oracle_sample_worker, ((args.config, k),))
+            wall, nb, tk = run.step(k)
             if i >= args.warmup:
-                times.append(dt)
+                times.append(wall)
                 nbytes, toks = nb, tk
+    finally:
+        run.close()
     total = sum(times)
     value = nbytes * len(times) / total / 1e9
-    sample = (f"first {k} of {len(ctx)} sequences of the workload per step (same recipe), "
-              "fp64 oracle: set-up append, step append and attention")
+    sample = (f"{cores} processes (one per host core), each the fp64 oracle step (set-up "
+              f"append, step append, attention) on its own {k} sequences of the workload's "
+              "recipe per step")
     line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * total / len(times), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": f"cfg{args.config}: {CONFIG_NAMES[args.config]}",
-                       "sample_seqs": k},
+                       "sample_seqs_per_core": k},
             "attended_tokens_per_s": toks * len(times) / total,
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample, "cpu": cpu_model()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -424,28 +497,37 @@ def run_reference(args):
 # ---------------------------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------------------------
-def run_ours(args):
-    import torch
-    rank, world, local = dist_env()
-    if args.gpus != world and world > 1:
-        print(f"--gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
-    device = torch.device("cuda", local)
-    torch.cuda.set_device(device)
-    dist = dist_init(world, "nccl")
-    from paged_kv_cache_286_gb300 import build
-    if rank == 0:
-        build.build()
-    barrier(dist, device)
-    import paged_kv_cache_286_gb300 as pa
-    from synthetic.workloads import CONFIG_NAMES, make_config
+def workload_for(config_id: int, seqs: int = 0):
+    from synthetic.workloads import config_lengths, make_config, make_workload
+    if seqs:
+        ctx, ql, kw = config_lengths(config_id)
+        return make_workload(ctx[:seqs], ql[:seqs], seed=1000 + config_id,
+                             name=f"cfg{config_id}-first{seqs}", **kw)
+    return make_config(config_id)
 
-    if args.seqs:
-        from synthetic.workloads import config_lengths, make_workload
-        ctx, ql, kw = config_lengths(args.config)
-        w = make_workload(ctx[:args.seqs], ql[:args.seqs], seed=1000 + args.config,
-                          name=f"cfg{args.config}-first{args.seqs}", **kw)
-    else:
-        w = make_config(args.config)
+
+def prefill_only(config_id: int):
+    """The sequences of a named workload whose query runs go to the tensor-core tiles, alone
+    (same lengths and recipe), or None when it has none."""
+    from synthetic.workloads import config_lengths, make_workload
+    ctx, ql, kw = config_lengths(config_id)
+    g = kw["num_q_heads"] // kw["num_kv_heads"]
+    if kw.get("cache_dtype", "bf16") != "bf16" or kw["head_dim"] != 128 or 128 % g:
+        return None
+    idx = [i for i, n in enumerate(ql) if n > 16 or n * g > 16]
+    if not idx or len(idx) == len(ql):
+        return None
+    kw = dict(kw)
+    kw.pop("num_blocks", None)
+    return make_workload([ctx[i] for i in idx], [ql[i] for i in idx], seed=1000 + config_id,
+                         name=f"cfg{config_id}-chunks", **kw)
+
+
+def measure(w, args, device, dist, world, sample_clocks=True):
+    """Times one workload's step: graph replays (value), eager steps with the library's kernel
+    events (roofline, prefill), and the end-to-end serving loop.  Returns a dict."""
+    import torch
+    import paged_kv_cache_286_gb300 as pa
     dw = DeviceWorkload(w, device)
     algo_attn = w.algorithmic_bytes()
     algo_step = algo_attn + w.append_bytes()
@@ -487,14 +569,15 @@ def run_ours(args):
         e.record(stream)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(device.index) if sample_clocks else None
     torch.cuda.synchronize(device)
     barrier(dist, device)
-    clocks.start()
+    if clocks:
+        clocks.start()
     # The sampler reads the clocks every 200 ms and the timed regions below last milliseconds:
     # replay the same step for about a second first, so that the samples are taken under this
     # load, which runs on into the timed regions without a pause.
-    t_end = time.monotonic() + 1.0
+    t_end = time.monotonic() + (1.0 if clocks else 0.1)
     while time.monotonic() < t_end:
         for _ in range(20):
             graph.replay()
@@ -519,9 +602,10 @@ def run_ours(args):
     g1.record(stream)
     torch.cuda.synchronize(device)
     barrier(dist, device)
-    clk = clocks.stop()
+    clk = clocks.stop() if clocks else None
     assert pa.check_error(dw.ws) == 0
-    kern_ms = statistics.mean(kb[i].elapsed_time(ka[i]) for i in range(K))
+    kern_ms = statistics.mean(kb[i].elapsed_time(ka[i]) for i in range(K)) if decode_seqs \
+        else None
     pf_flops = prefill_flops(w) if dw.has_prefill() else 0
     pf_ms = statistics.mean(pfb[i].elapsed_time(pfa[i]) for i in range(K)) if pf_flops else None
     step_ms = max_over_ranks(g0.elapsed_time(g1) / K, dist, device)
@@ -539,74 +623,124 @@ def run_ours(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K, dist, device)
     assert pa.check_error(dw.ws) == 0
 
-    peak, peak_kind, _ = load_peaks()
+    peak, peak_kind, peaks = load_peaks()
     value = world * algo_step / (step_ms * 1e-3) / 1e9
-    achieved = algo_decode / (kern_ms * 1e-3) / 1e9 if decode_seqs else 0.0
-    result = None
-    if rank == 0:
-        cpu = None
-        if not args.no_cpu_baseline:
-            s = oracle_sample(args.config, args.cpu_seconds)
-            cpu = {"value": s["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
-                   "sample": f"first {s['seqs']} of {s['of_seqs']} sequences of the workload "
-                             f"(same recipe), fp64 oracle step (set-up append, step append, "
-                             f"attention), {s['seconds']:.1f} s on one host core",
-                   "tokens_per_s": s["tokens_per_s"]}
-        result = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-            "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None,
-            "dtype": "e4m3" if w.cache_dtype == "fp8_e4m3" else "bf16", "data": "synthetic",
-            "config": {"workload": f"cfg{args.config}: {CONFIG_NAMES[args.config]}"
-                                   + (f" (first {args.seqs} sequences)" if args.seqs else ""),
-                       "l2": f"no flush: each step streams {algo_attn / 1e9:.2f} GB of K/V "
-                             "and q/out, far above the 129 MB L2",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-            "hbm_frac_of_peak": value / world / peak,
-            "timing": "CUDA graph of one step, replayed K times between CUDA events",
-            "eager_ms_per_step": eager_ms,
-            "attended_tokens_per_s": world * w.attended_tokens() / (step_ms * 1e-3),
-            "algorithmic_bytes_per_step": algo_step,
-            "e2e": {"value": world * algo_step / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
-                    "h2d_bytes_per_step": dw.h2d_bytes, "d2h_bytes_per_step": dw.d2h_bytes,
-                    "ms_per_step": e2e_ms,
-                    "copies": "one packed host-to-device copy of each step's inputs and one "
-                              "device-to-host copy of its output, on a copy stream, double-"
-                              "buffered against the steps' compute"},
-            "gpu_launches": K * dw.launches_per_step(),
-            "roofline": {"bound": "hbm", "kernel": "decode_kernel (split-KV paged attention)",
+    r = {
+        "workload": w.name, "dtype": "e4m3" if w.cache_dtype == "fp8_e4m3" else "bf16",
+        "ms_per_step": step_ms, "value": value, "unit": UNIT,
+        "hbm_frac_of_peak": value / world / peak, "eager_ms_per_step": eager_ms,
+        "attended_tokens_per_s": world * w.attended_tokens() / (step_ms * 1e-3),
+        "algorithmic_bytes_per_step": algo_step,
+        "e2e": {"value": world * algo_step / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+                "h2d_bytes_per_step": dw.h2d_bytes, "d2h_bytes_per_step": dw.d2h_bytes,
+                "ms_per_step": e2e_ms},
+        "gpu_launches_per_step": dw.launches_per_step(),
+        "clocks": clk,
+    }
+    if decode_seqs:
+        achieved = algo_decode / (kern_ms * 1e-3) / 1e9
+        r["roofline"] = {"bound": "hbm", "kernel": "decode_kernel (split-KV paged attention)",
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
-                         "traffic": traffic_from_profiles(args.config),
-                         "algorithmic_bytes_per_launch": algo_decode,
-                         "kernel_ms": kern_ms},
-            "cpu_baseline": cpu,
-            "clocks": clk,
-        }
-        if pf_flops and not decode_seqs:
+                         "traffic": None, "algorithmic_bytes_per_launch": algo_decode,
+                         "kernel_ms": kern_ms}
+    if pf_flops:
+        pf_peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+        pf_tf = pf_flops / (pf_ms * 1e-3) / 1e12
+        r["prefill"] = {
+            "bound": "tensor", "kernel": "prefill_kernel (tcgen05 causal tiles)",
+            "achieved": pf_tf, "peak": pf_peak, "unit": "TFLOP/s", "frac": pf_tf / pf_peak,
+            "peak_source": ("measured" if "bf16_tflops" in peaks else "fallback")
+                           + " bf16_tflops (burst)",
+            "flops_per_launch": pf_flops, "kernel_ms": pf_ms,
+            "algorithmic_bytes_per_launch": algo_prefill,
+            "achieved_gbs": algo_prefill / (pf_ms * 1e-3) / 1e9,
+            "flops": "algorithmic: 4 * head_dim * q heads * attended keys of the chunk "
+                     "queries (QK^T and PV); masked tile parts and the second (lo) half of P's "
+                     "bf16 split are extra MMA work not counted"}
+        if not decode_seqs:
             # every run of the step is on the tensor-core tiles (e.g. speculative verify with
             # GQA): that kernel is the dominant one, and it streams each K/V tile once
             pf_gbs = algo_prefill / (pf_ms * 1e-3) / 1e9
-            result["roofline"] = {
+            r["roofline"] = {
                 "bound": "hbm", "kernel": "prefill_kernel (tcgen05 causal tiles)",
                 "achieved": pf_gbs, "peak": peak, "unit": "GB/s", "frac": pf_gbs / peak,
                 "peak_source": f"{peak_kind} hbm_gbs", "traffic": None,
                 "algorithmic_bytes_per_launch": algo_prefill, "kernel_ms": pf_ms}
-        if pf_flops:
-            peaks = load_peaks()[2]
-            pf_peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
-            pf_tf = pf_flops / (pf_ms * 1e-3) / 1e12
-            result["prefill"] = {
-                "bound": "tensor", "kernel": "prefill_kernel (tcgen05 causal tiles)",
-                "achieved": pf_tf, "peak": pf_peak, "unit": "TFLOP/s", "frac": pf_tf / pf_peak,
-                "peak_source": ("measured" if "bf16_tflops" in peaks else "fallback")
-                               + " bf16_tflops (burst)",
-                "flops_per_launch": pf_flops, "kernel_ms": pf_ms,
-                "algorithmic_bytes_per_launch": algo_prefill,
-                "achieved_gbs": algo_prefill / (pf_ms * 1e-3) / 1e9,
-                "flops": "algorithmic: 4 * head_dim * q heads * attended keys of the chunk "
-                         "queries (QK^T and PV); masked tile parts and the second (lo) half "
-                         "of P's bf16 split are extra MMA work not counted"}
+    del graph, dw
+    torch.cuda.synchronize(device)
+    torch.cuda.empty_cache()
+    return r
+
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    if args.gpus != world and world > 1:
+        print(f"--gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist = dist_init(world, "nccl")
+    from paged_kv_cache_286_gb300 import build
+    if rank == 0:
+        build.build()
+    barrier(dist, device)
+    from synthetic.workloads import CONFIG_NAMES
+
+    headline = args.config if args.config else 2
+    w = workload_for(headline, args.seqs)
+    r = measure(w, args, device, dist, world)
+    r["roofline"]["traffic"] = None if args.seqs else traffic_from_profiles(headline)
+    per_config = None
+    if not args.config and not args.seqs:
+        # every named workload, one after the other, timed the same way
+        per_config = {}
+        for c in range(1, 7):
+            rc = r if c == headline else measure(workload_for(c), args, device, dist, world)
+            if "roofline" in rc:
+                rc["roofline"]["traffic"] = traffic_from_profiles(c)
+            if c == 1:
+                rc["note"] = ("launch-bound: 0.15 MB of K/V per step, a few microseconds of "
+                              "HBM time against the launch and plan latency of four kernels")
+            per_config[f"cfg{c}"] = rc
+        cfg4 = prefill_only(4)
+        if cfg4 is not None:
+            pr = measure(cfg4, args, device, dist, world, sample_clocks=False)
+            per_config["cfg4"]["prefill_alone"] = dict(
+                pr["prefill"], workload=cfg4.name, ms_per_step=pr["ms_per_step"],
+                note="the two prompt chunks of the mixed step without its decodes: the "
+                     "tensor-core kernel's own speed")
+    result = None
+    if rank == 0:
+        cpu = None if args.no_cpu_baseline else cpu_baseline(headline, args.cpu_seconds)
+        result = {
+            "metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": r["dtype"], "data": "synthetic",
+            "config": {"workload": f"cfg{headline}: {CONFIG_NAMES[headline]}"
+                                   + (f" (first {args.seqs} sequences)" if args.seqs else ""),
+                       "l2": f"no flush: each step streams "
+                             f"{r['algorithmic_bytes_per_step'] / 1e9:.2f} GB of K/V and q/out, "
+                             "far above the 129 MB L2",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "hbm_frac_of_peak": r["hbm_frac_of_peak"],
+            "timing": "CUDA graph of one step, replayed K times between CUDA events",
+            "eager_ms_per_step": r["eager_ms_per_step"],
+            "attended_tokens_per_s": r["attended_tokens_per_s"],
+            "algorithmic_bytes_per_step": r["algorithmic_bytes_per_step"],
+            "e2e": dict(r["e2e"], copies="one packed host-to-device copy of each step's inputs "
+                        "and one device-to-host copy of its output, on a copy stream, double-"
+                        "buffered against the steps' compute"),
+            "gpu_launches": args.steps * r["gpu_launches_per_step"],
+            "roofline": r["roofline"],
+            "cpu_baseline": cpu,
+            "clocks": r["clocks"],
+        }
+        if "prefill" in r:
+            result["prefill"] = r["prefill"]
+        if per_config is not None:
+            result["per_config"] = per_config
         print(json.dumps(result), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -616,6 +750,8 @@ def run_ours(args):
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
+        if not args.config:
+            args.config = 2
         return run_reference(args)
     return run_ours(args)
 

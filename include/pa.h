@@ -215,6 +215,28 @@ void pa_set_kernel_timing_events(void* before, void* after);
  * head_dim 128).  Pass NULLs to stop. */
 void pa_set_prefill_timing_events(void* before, void* after);
 
+/* Limit of every bounded device-side wait in the calling thread's later pa_attention calls, in
+ * nanoseconds of the GPU's global timer; 0 restores the default of 1 s.  A wait that reaches
+ * the limit gives up: the kernel sets PA_DEVERR_TIMEOUT, lets the copies it still has in flight
+ * land (each with its own bounded wait), and returns; pa_check_error then reports
+ * PA_ERR_TIMEOUT and that call's output is not valid.  (Not a step of the method: it bounds
+ * how long a lost copy can hold the GPU.) */
+void pa_set_wait_limit_ns(uint64_t ns);
+
+/* Test hook, off by default; never enable it outside tests.  While enabled, every pa_attention
+ * call of the calling thread leaves out exactly one tile copy of each attention kernel it
+ * launches (the first copy of the first work item claimed) while that copy's barrier still
+ * expects the bytes, so that the bounded waits on it expire and the call ends with
+ * PA_ERR_TIMEOUT without any fault: the expiry and drain paths of the kernels can be exercised
+ * on a real GPU. */
+void pa_test_skip_one_copy(int32_t enable);
+
+/* Self-test of the bounded wait: one thread waits, for limit_ns (in (0, 10 s]), on an mbarrier
+ * phase that nothing completes, then sets PA_DEVERR_TIMEOUT in the error word at the start of
+ * `workspace` (>= 4 bytes, device) and returns; read it with pa_check_error.  Asynchronous on
+ * `stream`.  (Not a step of the method: it checks the library's failure signal.) */
+pa_status pa_selftest_wait_timeout(void* workspace, uint64_t limit_ns, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

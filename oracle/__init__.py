@@ -28,3 +28,4 @@ from .paged_kv import (  # noqa: F401
     paged_attention,
     run_step,
 )
+from .parallel import cache_append_parallel, paged_attention_parallel  # noqa: F401,E402

@@ -59,6 +59,15 @@ def cache_append(k_pool: np.ndarray, v_pool: np.ndarray, k_bits: np.ndarray, v_b
     the table lookup has been folded into the slot: token t goes to block ``slot // block_size``
     at offset ``slot % block_size``, for every kv head.  Negative slots are skipped.
     """
+    return scatter_codes(k_pool, v_pool, _encode_cache(k_bits, cache_dtype, k_scale),
+                         _encode_cache(v_bits, cache_dtype, v_scale), slot_mapping, block_size)
+
+
+def scatter_codes(k_pool: np.ndarray, v_pool: np.ndarray, k_codes: np.ndarray,
+                  v_codes: np.ndarray, slot_mapping: np.ndarray, block_size: int):
+    """The write half of ``cache_append``: already encoded per-token codes ``[T][H][D]`` go to
+    block ``slot // block_size``, offset ``slot % block_size``; negative slots are skipped.
+    Returns new pool arrays."""
     k_out = k_pool.copy()
     v_out = v_pool.copy()
     slots = np.asarray(slot_mapping, dtype=np.int64)
@@ -69,8 +78,8 @@ def cache_append(k_pool: np.ndarray, v_pool: np.ndarray, k_bits: np.ndarray, v_b
     b = slots[keep] // block_size
     o = slots[keep] % block_size
     # one assignment per (token, kv head); a slot written twice in one call is undefined
-    k_out[b, :, o, :] = _encode_cache(np.asarray(k_bits)[keep], cache_dtype, k_scale)
-    v_out[b, :, o, :] = _encode_cache(np.asarray(v_bits)[keep], cache_dtype, v_scale)
+    k_out[b, :, o, :] = np.asarray(k_codes)[keep]
+    v_out[b, :, o, :] = np.asarray(v_codes)[keep]
     return k_out, v_out
 
 

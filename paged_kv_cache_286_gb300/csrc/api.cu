@@ -21,6 +21,8 @@ thread_local cudaEvent_t g_before = nullptr;
 thread_local cudaEvent_t g_after = nullptr;
 thread_local cudaEvent_t g_pf_before = nullptr;
 thread_local cudaEvent_t g_pf_after = nullptr;
+thread_local uint64_t g_wait_ns = pa::kWaitLimitNs;
+thread_local int32_t g_skip_copy = 0;
 
 pa_status fail(pa_status st, const char* fmt, ...) {
   char buf[512];
@@ -294,11 +296,27 @@ void pa_set_prefill_timing_events(void* before, void* after) {
   g_pf_after = static_cast<cudaEvent_t>(after);
 }
 
+void pa_set_wait_limit_ns(uint64_t ns) { g_wait_ns = ns ? ns : pa::kWaitLimitNs; }
+
+void pa_test_skip_one_copy(int32_t enable) { g_skip_copy = enable ? 1 : 0; }
+
 pa_status pa_workspace_init(void* workspace, cudaStream_t stream) {
   g_last_error.clear();
   if (!workspace) return fail(PA_ERR_INVALID_ARG, "workspace is NULL");
   cudaError_t e = cudaMemsetAsync(workspace, 0, PA_WORKSPACE_HEADER_BYTES, stream);
   if (e != cudaSuccess) return cuda_fail(e, "pa_workspace_init");
+  return PA_OK;
+}
+
+pa_status pa_selftest_wait_timeout(void* workspace, uint64_t limit_ns, cudaStream_t stream) {
+  g_last_error.clear();
+  if (!workspace) return fail(PA_ERR_INVALID_ARG, "workspace is NULL");
+  if (!aligned(workspace, 4)) return fail(PA_ERR_INVALID_ARG, "misaligned workspace");
+  if (limit_ns == 0 || limit_ns > 10ull * pa::kWaitLimitNs)
+    return fail(PA_ERR_INVALID_ARG, "limit_ns must be in (0, 10 s]");
+  cudaError_t e =
+      pa::launch_wait_timeout_selftest(static_cast<uint32_t*>(workspace), limit_ns, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "pa_selftest_wait_timeout launch");
   return PA_OK;
 }
 
@@ -412,6 +430,8 @@ pa_status pa_attention(const void* q, int32_t num_q_tokens, const void* k_cache,
                  workspace_bytes, stream};
   a.pf_before = g_pf_before;
   a.pf_after = g_pf_after;
+  a.wait_ns = g_wait_ns;
+  a.skip_copy = g_skip_copy;
   cudaError_t e =
       pa::launch_attention(a, ws, kmap, vmap, use_prefill ? &qmap : nullptr, g_before, g_after);
   if (e != cudaSuccess) return cuda_fail(e, "pa_attention launch");

@@ -69,6 +69,8 @@ struct DecodeParams {
   int32_t out_bf16;
   float score_log2;        // scale * log2(e) (* k_scale for E4M3)
   float v_out_scale;       // v_scale for E4M3, else 1
+  uint64_t wait_ns;        // limit of every bounded wait
+  int32_t skip_copy;       // test hook: item 0 leaves out its first tile copy (see pa.h)
 };
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -209,7 +211,7 @@ constexpr int decode_smem_bytes() {
 }
 
 struct ItemInfo {
-  int s, h, qt, part, t0, n, L, nparts, blk_begin, blk_end, pos_base, rows, valid;
+  int s, h, qt, part, t0, n, L, nparts, blk_begin, blk_end, pos_base, rows, valid, idx;
 };
 
 // The E4M3 two-head instance is held to 3 CTAs per SM (at most 170 registers a thread): it is
@@ -258,6 +260,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (kFp8 && HPI > 1) ? 3 : 1)
     ItemInfo info;
     const int item = static_cast<int>(atomicAdd(&p.hdr->decode_counter, 1u));
     info.valid = item < total_items;
+    info.idx = item;
     if (info.valid) {
       int lo = 0, hi = p.num_seqs;  // largest s with item_start[s] <= item
       while (hi - lo > 1) {
@@ -335,10 +338,15 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (kFp8 && HPI > 1) ? 3 : 1)
           uint8_t* vt = kt + C::kTileBytes;
           const int y = (phys * p.num_kv_heads + I.h) * kBlockSize;
           mbar_arrive_expect_tx(bar, C::kStageBytes);
+          // test hook: the first stage of the first item claimed (whichever CTA claims it)
+          // expects its bytes but gets no copy, so that the bounded wait on it expires
+          const bool skip = p.skip_copy && I.idx == 0 && warp == 0 && k == 0;
+          if (!skip) {
 #pragma unroll
-          for (int bx = 0; bx < C::kBoxes; ++bx) {
-            tma_load_2d(kt + bx * C::kBoxBytes, &kmap, bx * C::kBoxCols, y, bar);
-            tma_load_2d(vt + bx * C::kBoxBytes, &vmap, bx * C::kBoxCols, y, bar);
+            for (int bx = 0; bx < C::kBoxes; ++bx) {
+              tma_load_2d(kt + bx * C::kBoxBytes, &kmap, bx * C::kBoxCols, y, bar);
+              tma_load_2d(vt + bx * C::kBoxBytes, &vmap, bx * C::kBoxCols, y, bar);
+            }
           }
         } else {
           mbar_arrive(bar);
@@ -414,12 +422,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (kFp8 && HPI > 1) ? 3 : 1)
       const uint32_t st = it % NST;
       const uint32_t parity = (it / NST) & 1u;
       // every lane polls; the outcome is made warp-uniform before any lane acts on it
-      if (!__all_sync(0xffffffffu, mbar_wait(&wbars[st], parity))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&wbars[st], parity, p.wait_ns))) {
         if (lane == 0) set_error(&p.hdr->error, PA_DEVERR_TIMEOUT);
         timed_out = true;
         // drain the other loads in flight, each with its own bounded wait
         for (int k2 = k + 1; k2 < min(nb_w, k + NST); ++k2)
-          mbar_wait(&wbars[(it + (k2 - k)) % NST], ((it + (k2 - k)) / NST) & 1u);
+          mbar_wait(&wbars[(it + (k2 - k)) % NST], ((it + (k2 - k)) / NST) & 1u, p.wait_ns);
         break;
       }
       const int phys = __shfl_sync(0xffffffffu, phys_lane, k);
@@ -901,6 +909,8 @@ cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const CUtens
   p.decode_max_query = prefill ? kDecodeMaxQuery : INT32_MAX;
   p.decode_max_rows = prefill ? kDecodeMaxRows : INT32_MAX;
   p.out_bf16 = a.out_dtype == PA_BF16;
+  p.wait_ns = a.wait_ns;
+  p.skip_copy = a.skip_copy;
   const float log2e = 1.4426950408889634f;
   const bool fp8 = a.cache.cache_dtype == PA_FP8_E4M3;
   p.score_log2 = a.scale * log2e * (fp8 ? a.cache.k_scale : 1.f);

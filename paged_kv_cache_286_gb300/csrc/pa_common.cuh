@@ -36,7 +36,7 @@ __host__ __device__ constexpr bool routes_to_prefill(int n, int G) {
   return n > kDecodeMaxQuery || n * G > kDecodeMaxRows;
 }
 constexpr float kLazyRescaleLog2 = 8.f;  // softmax base moves only past 2^8 growth
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per bounded wait
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // default limit of a bounded wait
 
 __device__ __forceinline__ void set_error(uint32_t* err, uint32_t bits) {
   atomicOr(err, bits);
@@ -101,16 +101,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of `bar` to complete, giving up after kWaitLimitNs.  Returns false on
-// timeout (the caller records PA_DEVERR_TIMEOUT and stops using the buffer's contents).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Wait for phase `parity` of `bar` to complete, giving up after limit_ns of %globaltimer.
+// Returns false on timeout (the caller records PA_DEVERR_TIMEOUT and stops using the buffer's
+// contents).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   }
 }
 

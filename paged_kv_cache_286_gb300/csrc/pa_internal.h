@@ -53,6 +53,8 @@ struct AttnArgs {
   cudaStream_t stream;
   cudaEvent_t pf_before = nullptr;  // benchmark hook: recorded around the prefill kernel
   cudaEvent_t pf_after = nullptr;
+  uint64_t wait_ns = 0;             // limit of every bounded device-side wait
+  int32_t skip_copy = 0;            // test hook (pa_test_skip_one_copy)
 };
 
 // Workspace carve-up; a pure function of the step's shape (see workspace_layout).
@@ -87,6 +89,8 @@ pa_status check_attention_args(const void* q, int32_t num_q_tokens, const void* 
                                int32_t num_seqs, int32_t max_context_len, int32_t max_query_len,
                                int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                float scale, const void* out, int32_t out_dtype, bool* nothing);
+
+cudaError_t launch_wait_timeout_selftest(uint32_t* err, uint64_t limit_ns, cudaStream_t stream);
 
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const pa_cache_desc& c,
                                const int32_t* pairs, int32_t num_pairs, uint32_t* err,

@@ -86,10 +86,12 @@ struct PrefillParams {
   int32_t num_blocks;
   int32_t out_bf16;
   float score_log2;
+  uint64_t wait_ns;   // limit of every bounded wait
+  int32_t skip_copy;  // test hook: the first item claimed leaves out its first K copy
 };
 
 struct PfItem {
-  int s, h, t0, ntok, pos0, L, nkv, nblk_tile, valid;
+  int s, h, t0, ntok, pos0, L, nkv, nblk_tile, valid, first;
 };
 
 struct PfCtl {
@@ -170,7 +172,7 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
   };
   // all lanes wait; the outcome is warp-uniform
   auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, parity));
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, parity, p.wait_ns));
     if (!ok && lane == 0) fail(PA_DEVERR_TIMEOUT);
     return ok;
   };
@@ -181,6 +183,7 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
       const int rev = static_cast<int>(atomicAdd(&p.hdr->prefill_counter, 1u));
       const int item = total - 1 - rev;  // longest items (last tiles of a chunk) first
       it.valid = item >= 0;
+      it.first = rev == 0;
       if (it.valid) {
         int lo = 0, hi = p.num_seqs;
         while (hi - lo > 1) {
@@ -263,7 +266,10 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
           else mbar_arrive(&ctl->k_full[st]);
         }
         __syncwarp();
-        if (phys >= 0) {
+        // test hook: lane 0's copy of the first slice of the first item claimed is left out
+        // (its bytes are still expected), so that the bounded waits on that stage expire
+        const bool skip = p.skip_copy && I.first && j == 0 && lane == 0;
+        if (phys >= 0 && !skip) {
           const int yrow = (phys * p.num_kv_heads + I.h) * kBlockSize;
           uint8_t* kt = smem + pf::kK + st * pf::kTile + lane * 2048;
           tma_load_2d(kt, &kmap, 0, yrow, &ctl->k_full[st]);
@@ -601,6 +607,8 @@ cudaError_t launch_prefill(const AttnArgs& a, const int32_t* item_start, WsHeade
   p.num_blocks = a.cache.num_blocks;
   p.out_bf16 = a.out_dtype == PA_BF16;
   p.score_log2 = a.scale * 1.4426950408889634f;
+  p.wait_ns = a.wait_ns;
+  p.skip_copy = a.skip_copy;
   // Runs of at most 64 rows (tokens x group heads: speculative verify) leave at least two of
   // a tile's four lane quarters empty; splitting each row over two warps then puts a second
   // warp on the busy quarters' SM sub-partitions.  Fuller tiles gain nothing from the split.

@@ -223,3 +223,35 @@ def test_fp8_append_codes_match_torch_conversion():
     got = kp[slots // 16, :, slots % 16, :]
     assert np.array_equal(got, ref)
     assert np.abs(e4m3_decode(got)).max() <= 448
+
+
+def test_parallel_oracle_gives_the_serial_result_bitwise():
+    """paged_attention_parallel runs paged_attention itself on shares of the sequences in
+    spawned processes: its output must be the serial output, bit for bit, with the left-out
+    sequences' rows NaN in both."""
+    from oracle import paged_attention, paged_attention_parallel
+    from synthetic import make_workload
+    w = make_workload([40, 1, 300, 77, 16, 129], [1, 1, 9, 1, 16, 3], num_q_heads=8,
+                      num_kv_heads=2, head_dim=16, seed=11)
+    kp, vp = cache_append(w.empty_pool(), w.empty_pool(), w.k_prior_bits, w.v_prior_bits,
+                          w.slot_prior, w.block_size)
+    kp, vp = cache_append(kp, vp, w.k_new_bits, w.v_new_bits, w.slot_mapping, w.block_size)
+    args = (w.q_bits, kp, vp, w.block_tables, w.context_lens, w.query_start_loc, w.num_q_heads,
+            w.num_kv_heads, w.head_dim, w.scale, w.block_size)
+    for seqs in (None, [0, 2, 5]):
+        a = paged_attention(*args, seqs=seqs)
+        b = paged_attention_parallel(*args, seqs=seqs, processes=3)
+        assert np.array_equal(np.isnan(a), np.isnan(b))
+        assert np.array_equal(np.nan_to_num(a), np.nan_to_num(b))
+
+
+def test_parallel_e4m3_append_gives_the_serial_pools_bitwise():
+    from oracle import cache_append_parallel
+    from synthetic import make_workload
+    w = make_workload([300, 41, 700], [1, 1, 1], num_q_heads=4, num_kv_heads=2, head_dim=16,
+                      cache_dtype="fp8_e4m3", seed=12, pool_fill="nan")
+    args = (w.empty_pool(), w.empty_pool(), w.k_prior_bits, w.v_prior_bits, w.slot_prior,
+            w.block_size, w.cache_dtype, w.k_scale, w.v_scale)
+    a = cache_append(*args)
+    b = cache_append_parallel(*args, processes=3, rows_per_task=100)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
