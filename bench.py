@@ -61,6 +61,9 @@ def parse_args(argv=None):
     ap.add_argument("--seqs", type=int, default=0,
                     help="keep only the first N sequences of the workload (small profiling "
                          "cases; 0 = all)")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time only the workload's runs that go to the tensor-core prefill "
+                         "tiles (with --config)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="budget of the oracle CPU-baseline sample")
@@ -688,7 +691,7 @@ def run_ours(args):
     from synthetic.workloads import CONFIG_NAMES
 
     headline = args.config if args.config else 2
-    w = workload_for(headline, args.seqs)
+    w = prefill_only(headline) if args.prefill_only else workload_for(headline, args.seqs)
     r = measure(w, args, device, dist, world)
     r["roofline"]["traffic"] = None if args.seqs else traffic_from_profiles(headline)
     per_config = None

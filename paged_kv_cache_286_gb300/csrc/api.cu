@@ -77,6 +77,27 @@ pa_status encode_pool_map(CUtensorMap* map, const void* base, const pa_cache_des
   return PA_OK;
 }
 
+// 4-D view of a bf16 pool with head_dim 128 for whole-tile copies: (64 columns, 8 rows,
+// 2 column halves, 8-row groups) with byte strides (-, 256, 128, 2048).  One box of
+// {64, 8, 2, 2} is a (block, kv head) tile of 16 rows, landing in shared memory as
+// [2 row groups][2 halves][8 rows][128 bytes] with the 128-byte swizzle.
+pa_status encode_pool_tile_map(CUtensorMap* map, const void* base, const pa_cache_desc& c) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t rows = static_cast<cuuint64_t>(c.num_blocks) * c.num_kv_heads *
+                          static_cast<cuuint64_t>(c.block_size);
+  const cuuint64_t dims[4] = {64, 8, 2, rows / 8};
+  const cuuint64_t strides[3] = {256, 128, 2048};
+  const cuuint32_t box[4] = {64, 8, 2, 2};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled (pool tiles) failed (%d)", int(r));
+  return PA_OK;
+}
+
 // 3-D view of q [T][Hq][D] bf16; one box = (64 columns, G heads, 128 / G tokens) = 128 rows
 // of 128 bytes with the 128-byte swizzle, the q tile of one prefill work item.
 pa_status encode_q_map(CUtensorMap* map, const void* q, int32_t T, int32_t Hq, int32_t D,
@@ -409,20 +430,26 @@ pa_status pa_attention(const void* q, int32_t num_q_tokens, const void* k_cache,
   if (workspace_bytes < ws.total)
     return fail(PA_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes,
                 ws.total);
-  CUtensorMap kmap, vmap;
+  pa::PoolMaps maps;
   // boxes of one or two kv heads' rows (two only for single-token E4M3 decode, where no
   // prefill tile reads these maps)
   const int hpi = pa::decode_heads_per_item(*cache, num_q_heads, num_kv_heads, max_query_len);
-  if ((st = encode_pool_map(&kmap, k_cache, *cache, hpi)) != PA_OK) return st;
-  if ((st = encode_pool_map(&vmap, v_cache, *cache, hpi)) != PA_OK) return st;
+  if ((st = encode_pool_map(&maps.k2, k_cache, *cache, hpi)) != PA_OK) return st;
+  if ((st = encode_pool_map(&maps.v2, v_cache, *cache, hpi)) != PA_OK) return st;
 
-  CUtensorMap qmap;
+  const int32_t G = num_q_heads / num_kv_heads;
   const bool use_prefill = pa::prefill_path_enabled(*cache, num_q_heads, num_kv_heads) &&
-                           pa::routes_to_prefill(max_query_len, num_q_heads / num_kv_heads);
-  if (use_prefill &&
-      (st = encode_q_map(&qmap, q, num_q_tokens, num_q_heads, head_dim,
-                         num_q_heads / num_kv_heads)) != PA_OK)
-    return st;
+                           pa::routes_to_prefill(max_query_len, G);
+  if (use_prefill) {
+    if ((st = encode_q_map(&maps.q3, q, num_q_tokens, num_q_heads, head_dim, G)) != PA_OK)
+      return st;
+    maps.has_q3 = true;
+    if (pa::prefill_uses_pairs(max_query_len, G)) {
+      if ((st = encode_pool_tile_map(&maps.k4, k_cache, *cache)) != PA_OK) return st;
+      if ((st = encode_pool_tile_map(&maps.v4, v_cache, *cache)) != PA_OK) return st;
+      maps.has_k4 = true;
+    }
+  }
 
   pa::AttnArgs a{q, num_q_tokens, k_cache, v_cache, *cache, block_tables, max_blocks_per_seq,
                  context_lens, query_start_loc, num_seqs, max_context_len, max_query_len,
@@ -432,8 +459,7 @@ pa_status pa_attention(const void* q, int32_t num_q_tokens, const void* k_cache,
   a.pf_after = g_pf_after;
   a.wait_ns = g_wait_ns;
   a.skip_copy = g_skip_copy;
-  cudaError_t e =
-      pa::launch_attention(a, ws, kmap, vmap, use_prefill ? &qmap : nullptr, g_before, g_after);
+  cudaError_t e = pa::launch_attention(a, ws, maps, use_prefill, g_before, g_after);
   if (e != cudaSuccess) return cuda_fail(e, "pa_attention launch");
   return PA_OK;
 }

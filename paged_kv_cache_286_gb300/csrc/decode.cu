@@ -66,6 +66,7 @@ struct DecodeParams {
   int32_t decode_max_rows;   // so do runs of more (token x head) rows than one decode tile
   int32_t rows_per_tile;   // 8 * RT of the decode kernel instance
   int32_t heads_per_item;  // HPI of the decode kernel instance
+  int32_t pf_pairs;        // prefill items are pairs of 128-row tiles (else single tiles)
   int32_t out_bf16;
   float score_log2;        // scale * log2(e) (* k_scale for E4M3)
   float v_out_scale;       // v_scale for E4M3, else 1
@@ -99,12 +100,14 @@ __device__ __forceinline__ int decode_items_of(const DecodeParams& p, int n, int
   return p.num_kv_heads / p.heads_per_item * qtiles * nparts;
 }
 
-// Prefill-path items of one sequence: one per (kv head, 128-row tile of tokens x heads).
+// Prefill-path items of one sequence: one per (kv head, 128-row tile of tokens x heads), or
+// per (kv head, pair of consecutive tiles) for the two-tile chunk kernel.
 __device__ __forceinline__ int prefill_items_of(const DecodeParams& p, int n, int L) {
   bool bad;
   if (decode_items_of(p, n, L, &bad) != 0 || bad || n <= 0) return 0;
   const int tpt = 128 / p.group;
-  return p.num_kv_heads * ceil_div(n, tpt);
+  const int tiles = ceil_div(n, tpt);
+  return p.num_kv_heads * (p.pf_pairs ? ceil_div(tiles, 2) : tiles);
 }
 
 // One CTA: exclusive prefix sums over sequences of decode items, prefill items and merge rows
@@ -870,9 +873,10 @@ bool prefill_path_enabled(const pa_cache_desc& c, int32_t num_q_heads, int32_t n
          128 % G == 0;
 }
 
-cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const CUtensorMap& kmap,
-                             const CUtensorMap& vmap, const CUtensorMap* qmap,
-                             cudaEvent_t before, cudaEvent_t after) {
+cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const PoolMaps& maps,
+                             bool use_prefill, cudaEvent_t before, cudaEvent_t after) {
+  const CUtensorMap& kmap = maps.k2;
+  const CUtensorMap& vmap = maps.v2;
   uint8_t* wsb = static_cast<uint8_t*>(a.workspace);
   DecodeParams p{};
   p.q = static_cast<const __nv_bfloat16*>(a.q);
@@ -904,8 +908,9 @@ cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const CUtens
   p.heads_per_item = hpi;
   p.pblk = (fp8_cache && ws.pblk <= 32) ? ws.pblk * 2 : ws.pblk;
   p.pmax = ws.pmax;
-  const bool prefill = qmap != nullptr && prefill_path_enabled(a.cache, a.num_q_heads,
-                                                               a.num_kv_heads);
+  const bool prefill = use_prefill && prefill_path_enabled(a.cache, a.num_q_heads,
+                                                          a.num_kv_heads);
+  p.pf_pairs = prefill && prefill_uses_pairs(a.max_query_len, p.group) ? 1 : 0;
   p.decode_max_query = prefill ? kDecodeMaxQuery : INT32_MAX;
   p.decode_max_rows = prefill ? kDecodeMaxRows : INT32_MAX;
   p.out_bf16 = a.out_dtype == PA_BF16;
@@ -938,8 +943,7 @@ cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const CUtens
     if ((e = cudaStreamWaitEvent(side.stream, side.fork, 0)) != cudaSuccess) return e;
     AttnArgs b = a;
     b.stream = side.stream;
-    if ((e = launch_prefill(b, p.pf_item_start, p.hdr, *qmap, kmap, vmap)) != cudaSuccess)
-      return e;
+    if ((e = launch_prefill(b, p.pf_item_start, p.hdr, maps)) != cudaSuccess) return e;
     if ((e = cudaEventRecord(side.join, side.stream)) != cudaSuccess) return e;
   }
   if (fp8 && hpi == 2)

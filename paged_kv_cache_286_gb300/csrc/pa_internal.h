@@ -125,11 +125,32 @@ inline cudaError_t launch_dependent(void (*kern)(Params...), dim3 grid, dim3 blo
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
-cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const CUtensorMap& kmap,
-                             const CUtensorMap& vmap, const CUtensorMap* qmap,
-                             cudaEvent_t before, cudaEvent_t after);
+struct PoolMaps;
+cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const PoolMaps& maps,
+                             bool prefill, cudaEvent_t before, cudaEvent_t after);
 
 struct WsHeader;
+
+// Parameters of the tensor-core prefill kernels (prefill.cu, chunk.cu).
+struct PrefillParams {
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const int32_t* qsl;
+  const int32_t* item_start;  // [S+1] prefix sums of prefill items
+  void* out;
+  WsHeader* hdr;
+  int32_t max_blocks_per_seq;
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t group;
+  int32_t num_blocks;
+  int32_t out_bf16;
+  float score_log2;
+  uint64_t wait_ns;   // limit of every bounded wait
+  int32_t skip_copy;  // test hook: the first item claimed leaves out its first K copy
+};
+
 // A high-priority stream of the current device for the prefill-tile kernel, and two events of
 // the calling thread to fork it from and join it to the caller's stream.  Created on first use
 // (per device; the events per thread and device) and kept for the life of the process.
@@ -140,8 +161,22 @@ struct SideStream {
 };
 cudaError_t side_stream(SideStream* out);
 
+// Tensor maps of one call: the pool as 2-D rows (split-KV kernel, verify tiles), the pool as
+// 4-D whole (block, kv head) tiles and q as 3-D tiles (prefill kernels; NULL when unused).
+struct PoolMaps {
+  CUtensorMap k2, v2, k4, v4, q3;
+  bool has_k4 = false, has_q3 = false;
+};
+
+// Whether the step's prefill runs take the two-tile chunk kernel (runs of more than 64 rows)
+// rather than the one-tile verify kernel with rows split over two warps.
+inline bool prefill_uses_pairs(int32_t max_query_len, int32_t group) {
+  return static_cast<int64_t>(max_query_len) * group > 64;
+}
+
 cudaError_t launch_prefill(const AttnArgs& a, const int32_t* item_start, WsHeader* hdr,
-                           const CUtensorMap& qmap, const CUtensorMap& kmap,
-                           const CUtensorMap& vmap);
+                           const PoolMaps& maps);
+cudaError_t launch_chunk(const AttnArgs& a, const PrefillParams& p, const CUtensorMap& qmap,
+                         const CUtensorMap& kmap4, const CUtensorMap& vmap4);
 
 }  // namespace pa

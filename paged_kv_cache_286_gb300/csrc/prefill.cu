@@ -71,24 +71,6 @@ constexpr uint32_t kOCol = kSBufs * 128;
 constexpr float kRescaleLog2 = 8.f;
 }  // namespace pf
 
-struct PrefillParams {
-  const int32_t* block_tables;
-  const int32_t* context_lens;
-  const int32_t* qsl;
-  const int32_t* item_start;  // [S+1] prefix sums of prefill items
-  void* out;
-  WsHeader* hdr;
-  int32_t max_blocks_per_seq;
-  int32_t num_seqs;
-  int32_t num_q_heads;
-  int32_t num_kv_heads;
-  int32_t group;
-  int32_t num_blocks;
-  int32_t out_bf16;
-  float score_log2;
-  uint64_t wait_ns;   // limit of every bounded wait
-  int32_t skip_copy;  // test hook: the first item claimed leaves out its first K copy
-};
 
 struct PfItem {
   int s, h, t0, ntok, pos0, L, nkv, nblk_tile, valid, first;
@@ -590,8 +572,7 @@ cudaError_t launch_prefill_as(const AttnArgs& a, const PrefillParams& p, const C
 }  // namespace
 
 cudaError_t launch_prefill(const AttnArgs& a, const int32_t* item_start, WsHeader* hdr,
-                           const CUtensorMap& qmap, const CUtensorMap& kmap,
-                           const CUtensorMap& vmap) {
+                           const PoolMaps& maps) {
   PrefillParams p{};
   p.block_tables = a.block_tables;
   p.context_lens = a.context_lens;
@@ -612,9 +593,9 @@ cudaError_t launch_prefill(const AttnArgs& a, const int32_t* item_start, WsHeade
   // Runs of at most 64 rows (tokens x group heads: speculative verify) leave at least two of
   // a tile's four lane quarters empty; splitting each row over two warps then puts a second
   // warp on the busy quarters' SM sub-partitions.  Fuller tiles gain nothing from the split.
-  if (static_cast<int64_t>(a.max_query_len) * p.group <= 64)
-    return launch_prefill_as<true>(a, p, qmap, kmap, vmap);
-  return launch_prefill_as<false>(a, p, qmap, kmap, vmap);
+  if (!prefill_uses_pairs(a.max_query_len, p.group))
+    return launch_prefill_as<true>(a, p, maps.q3, maps.k2, maps.v2);
+  return launch_chunk(a, p, maps.q3, maps.k4, maps.v4);
 }
 
 }  // namespace pa
