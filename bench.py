@@ -585,14 +585,24 @@ def measure(w, args, device, dist, world, sample_clocks=True):
         for _ in range(20):
             graph.replay()
         torch.cuda.synchronize(device)
-    # (1) eager steps, with the main attention kernel bracketed by events for the roofline
+    # (1) eager steps with the library's span hook: the global-timer start and end of the
+    # split-KV and prefill-tile kernels as they run in the step (overlapping each other)
+    spans = torch.tensor([-1, 0, -1, 0] * K, dtype=torch.int64, device=device)
     torch.cuda.synchronize(device)
     start.record(stream)
+    for i in range(K):
+        pa.set_kernel_span_buffer(spans[4 * i:4 * i + 4])
+        dw.step()
+    stop.record(stream)
+    torch.cuda.synchronize(device)
+    pa.set_kernel_span_buffer(None)
+    sp = spans.view(K, 4).cpu().numpy().astype(np.uint64)
+    # (2) eager steps with events around each of the two kernels: the events make each
+    # kernel wait for the one before it, so these time every kernel alone
     for i in range(K):
         pa.set_kernel_timing_events(kb[i], ka[i])
         pa.set_prefill_timing_events(pfb[i], pfa[i])
         dw.step()
-    stop.record(stream)
     torch.cuda.synchronize(device)
     pa.set_kernel_timing_events(None, None)
     pa.set_prefill_timing_events(None, None)
@@ -607,10 +617,18 @@ def measure(w, args, device, dist, world, sample_clocks=True):
     barrier(dist, device)
     clk = clocks.stop() if clocks else None
     assert pa.check_error(dw.ws) == 0
-    kern_ms = statistics.mean(kb[i].elapsed_time(ka[i]) for i in range(K)) if decode_seqs \
-        else None
+    def span_ms(col):
+        v = [float(sp[i, col + 1] - sp[i, col]) * 1e-6 for i in range(K)
+             if sp[i, col] != np.uint64(2 ** 64 - 1) and sp[i, col + 1] >= sp[i, col]]
+        return statistics.mean(v) if v else None
+
+    kern_ms = span_ms(0) if decode_seqs else None
+    kern_alone_ms = statistics.mean(kb[i].elapsed_time(ka[i]) for i in range(K)) \
+        if decode_seqs else None
     pf_flops = prefill_flops(w) if dw.has_prefill() else 0
-    pf_ms = statistics.mean(pfb[i].elapsed_time(pfa[i]) for i in range(K)) if pf_flops else None
+    pf_ms = span_ms(2) if pf_flops else None
+    pf_alone_ms = statistics.mean(pfb[i].elapsed_time(pfa[i]) for i in range(K)) \
+        if pf_flops else None
     step_ms = max_over_ranks(g0.elapsed_time(g1) / K, dist, device)
     eager_ms = max_over_ranks(start.elapsed_time(stop) / K, dist, device)
 
@@ -642,20 +660,29 @@ def measure(w, args, device, dist, world, sample_clocks=True):
     }
     if decode_seqs:
         achieved = algo_decode / (kern_ms * 1e-3) / 1e9
+        alone = algo_decode / (kern_alone_ms * 1e-3) / 1e9
         r["roofline"] = {"bound": "hbm", "kernel": "decode_kernel (split-KV paged attention)",
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
                          "traffic": None, "algorithmic_bytes_per_launch": algo_decode,
-                         "kernel_ms": kern_ms}
+                         "kernel_ms": kern_ms,
+                         "timing": "span of the kernel in the step (first CTA start to last "
+                                   "CTA end, device global timer)",
+                         "kernel_ms_alone": kern_alone_ms, "achieved_alone": alone,
+                         "frac_alone": alone / peak}
     if pf_flops:
         pf_peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
         pf_tf = pf_flops / (pf_ms * 1e-3) / 1e12
+        pf_tf_alone = pf_flops / (pf_alone_ms * 1e-3) / 1e12
         r["prefill"] = {
-            "bound": "tensor", "kernel": "prefill_kernel (tcgen05 causal tiles)",
+            "bound": "tensor", "kernel": "prefill tiles (tcgen05 causal tiles)",
             "achieved": pf_tf, "peak": pf_peak, "unit": "TFLOP/s", "frac": pf_tf / pf_peak,
             "peak_source": ("measured" if "bf16_tflops" in peaks else "fallback")
                            + " bf16_tflops (burst)",
             "flops_per_launch": pf_flops, "kernel_ms": pf_ms,
+            "timing": "span of the kernel in the step (device global timer)",
+            "kernel_ms_alone": pf_alone_ms, "achieved_alone": pf_tf_alone,
+            "frac_alone": pf_tf_alone / pf_peak,
             "algorithmic_bytes_per_launch": algo_prefill,
             "achieved_gbs": algo_prefill / (pf_ms * 1e-3) / 1e9,
             "flops": "algorithmic: 4 * head_dim * q heads * attended keys of the chunk "
@@ -670,6 +697,9 @@ def measure(w, args, device, dist, world, sample_clocks=True):
                 "achieved": pf_gbs, "peak": peak, "unit": "GB/s", "frac": pf_gbs / peak,
                 "peak_source": f"{peak_kind} hbm_gbs", "traffic": None,
                 "algorithmic_bytes_per_launch": algo_prefill, "kernel_ms": pf_ms}
+    if pf_flops:
+        # the plan's SM budget for the prefill tiles (workspace header word 3)
+        r["prefill"]["ctas"] = int(dw.ws[12:16].cpu().view(torch.int32).item())
     del graph, dw
     torch.cuda.synchronize(device)
     torch.cuda.empty_cache()

@@ -145,12 +145,13 @@ size_t pa_attention_workspace_size(int32_t num_seqs, int32_t num_q_tokens, int32
  *                 first PA_WORKSPACE_HEADER_BYTES hold the error word.
  * A sequence with n_s == 0 produces nothing.  Accumulation is fp32; scores use exp2 of
  * log2(e)-prescaled logits.
- * Streams: with a bf16 pool of head_dim 128, query runs of more than 16 tokens or more than 16
- * (token x q head) rows are computed by a tensor-core kernel on a high-priority side stream of
- * the calling thread, forked from `stream` by an event and joined back into it before the call
- * returns, so all of the call's work stays ordered on `stream` (and is captured with it into a
- * CUDA graph).  The first such call of a thread on a device creates that stream and its two
- * events; make it before any stream capture. */
+ * Kernels: every kernel of the call runs on `stream`, each launched early (programmatic
+ * dependent launch) and waiting for what it reads: a plan, then, with a bf16 pool of head_dim
+ * 128 and query runs of more than 16 tokens or more than 16 (token x q head) rows, the
+ * tensor-core prefill tiles on the part of the SMs the plan gives them, the split-KV kernel on
+ * the rest, and the merge of split sequences.  Work enqueued on `stream` after the call sees
+ * all of it complete.  The call records no event and creates no stream, so it can be captured
+ * into a CUDA graph like any kernel launch. */
 pa_status pa_attention(const void* q, int32_t num_q_tokens, const void* k_cache,
                        const void* v_cache, const pa_cache_desc* cache,
                        const int32_t* block_tables, int32_t max_blocks_per_seq,
@@ -207,13 +208,23 @@ const char* pa_version(void);
 
 /* Benchmark hook.  When both events are non-NULL (cudaEvent_t handles), every later
  * pa_attention call of the calling thread records `before` immediately before, and `after`
- * immediately after, its main attention kernel, on the call's stream.  Pass NULLs to stop. */
+ * immediately after, its split-KV attention kernel, on the call's stream.  An event between
+ * two of the call's kernels makes the later one wait for the earlier one to finish, so with
+ * these events the kernels run one after the other and each is timed alone.  Pass NULLs to
+ * stop. */
 void pa_set_kernel_timing_events(void* before, void* after);
 
 /* Benchmark hook, like pa_set_kernel_timing_events, for the tensor-core prefill-tile kernel
- * (launched only by steps that hold chunks of more than 16 queries over a bf16 pool with
- * head_dim 128).  Pass NULLs to stop. */
+ * (launched only by steps that hold runs of more than 16 tokens or 16 token x head rows over a
+ * bf16 pool with head_dim 128).  Pass NULLs to stop. */
 void pa_set_prefill_timing_events(void* before, void* after);
+
+/* Benchmark hook that times kernels while they overlap: when `device_buffer` is non-NULL
+ * (four uint64_t in device memory, set by the caller to {UINT64_MAX, 0, UINT64_MAX, 0}), every
+ * later pa_attention call of the calling thread has its split-KV kernel lower [0] to the
+ * GPU's global timer (ns) when a CTA starts and raise [1] to it when a CTA finishes its work,
+ * and its prefill-tile kernel do the same with [2] and [3].  Pass NULL to stop. */
+void pa_set_kernel_span_buffer(uint64_t* device_buffer);
 
 /* Limit of every bounded device-side wait in the calling thread's later pa_attention calls, in
  * nanoseconds of the GPU's global timer; 0 restores the default of 1 s.  A wait that reaches

@@ -25,7 +25,7 @@ from ._lib import (PA_BF16, PA_FP8_E4M3, PA_FP32, PA_WORKSPACE_HEADER_BYTES,  # 
 
 __all__ = ["cache_append", "attention", "attention_workspace_size", "new_workspace",
            "check_error", "library", "version", "PagedAttnError", "set_kernel_timing_events",
-           "set_prefill_timing_events"]
+           "set_prefill_timing_events", "set_kernel_span_buffer"]
 
 
 def library() -> ctypes.CDLL:
@@ -157,6 +157,17 @@ def set_kernel_timing_events(before: Optional[torch.cuda.Event],
     b = ctypes.c_void_p(before.cuda_event) if before is not None else ctypes.c_void_p(0)
     a = ctypes.c_void_p(after.cuda_event) if after is not None else ctypes.c_void_p(0)
     _lib.load().pa_set_kernel_timing_events(b, a)
+
+
+def set_kernel_span_buffer(buf: Optional[torch.Tensor]) -> None:
+    """Have later attention calls of this thread record the global-timer span (ns) of their
+    split-KV kernel into buf[0:2] and of their prefill-tile kernel into buf[2:4] (int64 CUDA
+    tensor preset to [-1, 0, -1, 0], read as unsigned); None stops (benchmark hook)."""
+    if buf is not None:
+        _need(buf, "span buffer", (torch.int64,), 1)
+        if buf.numel() < 4:
+            raise ValueError("the span buffer needs four entries")
+    _lib.load().pa_set_kernel_span_buffer(_ptr(buf) if buf is not None else ctypes.c_void_p(0))
 
 
 def set_prefill_timing_events(before: Optional[torch.cuda.Event],

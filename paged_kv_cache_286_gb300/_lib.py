@@ -21,7 +21,8 @@ STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED",
 EXPORTED = ["pa_cache_append", "pa_attention_workspace_size", "pa_attention", "pa_check_error",
             "pa_workspace_init", "pa_last_error_string", "pa_version",
             "pa_set_kernel_timing_events", "pa_set_prefill_timing_events",
-            "pa_attention_noalloc", "pa_copy_blocks", "pa_set_wait_limit_ns",
+            "pa_attention_noalloc", "pa_copy_blocks", "pa_set_kernel_span_buffer",
+            "pa_set_wait_limit_ns",
             "pa_test_skip_one_copy", "pa_selftest_wait_timeout"]
 EXPORTED_BM = ["pa_bm_create", "pa_bm_destroy", "pa_bm_num_free", "pa_bm_append",
                "pa_bm_append_tokens", "pa_bm_fork", "pa_bm_free", "pa_bm_block_table",
@@ -104,6 +105,8 @@ def load() -> ctypes.CDLL:
     L.pa_set_kernel_timing_events.restype = None
     L.pa_set_prefill_timing_events.argtypes = [vp, vp]
     L.pa_set_prefill_timing_events.restype = None
+    L.pa_set_kernel_span_buffer.argtypes = [vp]
+    L.pa_set_kernel_span_buffer.restype = None
     L.pa_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     L.pa_set_wait_limit_ns.restype = None
     L.pa_test_skip_one_copy.argtypes = [i32]

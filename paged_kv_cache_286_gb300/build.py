@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpagedattn.so")
 SOURCES = ["api.cu", "append.cu", "decode.cu", "noalloc.cu", "prefill.cu", "copy.cu",
-           "chunk.cu", "selftest.cu", "block_manager.cpp"]
+           "selftest.cu", "block_manager.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

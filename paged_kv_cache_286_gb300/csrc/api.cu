@@ -21,6 +21,7 @@ thread_local cudaEvent_t g_before = nullptr;
 thread_local cudaEvent_t g_after = nullptr;
 thread_local cudaEvent_t g_pf_before = nullptr;
 thread_local cudaEvent_t g_pf_after = nullptr;
+thread_local uint64_t* g_span = nullptr;
 thread_local uint64_t g_wait_ns = pa::kWaitLimitNs;
 thread_local int32_t g_skip_copy = 0;
 
@@ -221,40 +222,6 @@ cudaError_t launch_info_impl(const void* kern, int threads, int smem_bytes, Laun
   return cudaSuccess;
 }
 
-cudaError_t side_stream(SideStream* out) {
-  // per thread and device, so that concurrent callers on other threads never wait on each
-  // other's prefill kernels
-  constexpr int kMaxDev = 64;
-  thread_local cudaStream_t streams[kMaxDev] = {};
-  thread_local cudaEvent_t forks[kMaxDev] = {};
-  thread_local cudaEvent_t joins[kMaxDev] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
-  if (!streams[dev]) {
-    int least = 0, greatest = 0;
-    if ((e = cudaDeviceGetStreamPriorityRange(&least, &greatest)) != cudaSuccess) return e;
-    if ((e = cudaStreamCreateWithPriority(&streams[dev], cudaStreamNonBlocking, greatest)) !=
-        cudaSuccess) {
-      streams[dev] = nullptr;
-      return e;
-    }
-  }
-  if (!forks[dev] && (e = cudaEventCreateWithFlags(&forks[dev], cudaEventDisableTiming)) !=
-                         cudaSuccess) {
-    forks[dev] = nullptr;
-    return e;
-  }
-  if (!joins[dev] && (e = cudaEventCreateWithFlags(&joins[dev], cudaEventDisableTiming)) !=
-                         cudaSuccess) {
-    joins[dev] = nullptr;
-    return e;
-  }
-  *out = SideStream{streams[dev], forks[dev], joins[dev]};
-  return cudaSuccess;
-}
-
 // Lets other translation units of the library report a host-side error through
 // pa_last_error_string.
 void set_last_error(const char* msg) { g_last_error = msg; }
@@ -316,6 +283,8 @@ void pa_set_prefill_timing_events(void* before, void* after) {
   g_pf_before = static_cast<cudaEvent_t>(before);
   g_pf_after = static_cast<cudaEvent_t>(after);
 }
+
+void pa_set_kernel_span_buffer(uint64_t* device_buffer) { g_span = device_buffer; }
 
 void pa_set_wait_limit_ns(uint64_t ns) { g_wait_ns = ns ? ns : pa::kWaitLimitNs; }
 
@@ -444,11 +413,9 @@ pa_status pa_attention(const void* q, int32_t num_q_tokens, const void* k_cache,
     if ((st = encode_q_map(&maps.q3, q, num_q_tokens, num_q_heads, head_dim, G)) != PA_OK)
       return st;
     maps.has_q3 = true;
-    if (pa::prefill_uses_pairs(max_query_len, G)) {
-      if ((st = encode_pool_tile_map(&maps.k4, k_cache, *cache)) != PA_OK) return st;
-      if ((st = encode_pool_tile_map(&maps.v4, v_cache, *cache)) != PA_OK) return st;
-      maps.has_k4 = true;
-    }
+    if ((st = encode_pool_tile_map(&maps.k4, k_cache, *cache)) != PA_OK) return st;
+    if ((st = encode_pool_tile_map(&maps.v4, v_cache, *cache)) != PA_OK) return st;
+    maps.has_k4 = true;
   }
 
   pa::AttnArgs a{q, num_q_tokens, k_cache, v_cache, *cache, block_tables, max_blocks_per_seq,
@@ -459,6 +426,7 @@ pa_status pa_attention(const void* q, int32_t num_q_tokens, const void* k_cache,
   a.pf_after = g_pf_after;
   a.wait_ns = g_wait_ns;
   a.skip_copy = g_skip_copy;
+  a.span = g_span;
   cudaError_t e = pa::launch_attention(a, ws, maps, use_prefill, g_before, g_after);
   if (e != cudaSuccess) return cuda_fail(e, "pa_attention launch");
   return PA_OK;

@@ -66,10 +66,13 @@ struct DecodeParams {
   int32_t decode_max_rows;   // so do runs of more (token x head) rows than one decode tile
   int32_t rows_per_tile;   // 8 * RT of the decode kernel instance
   int32_t heads_per_item;  // HPI of the decode kernel instance
-  int32_t pf_pairs;        // prefill items are pairs of 128-row tiles (else single tiles)
   int32_t out_bf16;
   float score_log2;        // scale * log2(e) (* k_scale for E4M3)
   float v_out_scale;       // v_scale for E4M3, else 1
+  uint64_t* span;          // benchmark hook: [first CTA start, last CTA end] in ns, or NULL
+  int32_t wait_at_end;     // launched after the prefill kernel: wait for it only at the end
+  int32_t sms;             // SMs of the device (the plan's SM split)
+  int32_t kv_tile_bytes;   // bytes of one (block, kv head) tile of K plus V
   uint64_t wait_ns;        // limit of every bounded wait
   int32_t skip_copy;       // test hook: item 0 leaves out its first tile copy (see pa.h)
 };
@@ -100,14 +103,13 @@ __device__ __forceinline__ int decode_items_of(const DecodeParams& p, int n, int
   return p.num_kv_heads / p.heads_per_item * qtiles * nparts;
 }
 
-// Prefill-path items of one sequence: one per (kv head, 128-row tile of tokens x heads), or
-// per (kv head, pair of consecutive tiles) for the two-tile chunk kernel.
+// Prefill-path items of one sequence: one per (kv head, 128-row tile of tokens x heads, key
+// split of the tile).
 __device__ __forceinline__ int prefill_items_of(const DecodeParams& p, int n, int L) {
   bool bad;
   if (decode_items_of(p, n, L, &bad) != 0 || bad || n <= 0) return 0;
   const int tpt = 128 / p.group;
-  const int tiles = ceil_div(n, tpt);
-  return p.num_kv_heads * (p.pf_pairs ? ceil_div(tiles, 2) : tiles);
+  return p.num_kv_heads * ceil_div(n, tpt) * prefill_splits(n, L, p.group, p.pmax);
 }
 
 // One CTA: exclusive prefix sums over sequences of decode items, prefill items and merge rows
@@ -124,8 +126,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
   constexpr int kN = 3;      // decode items, prefill items, merge rows
   __shared__ int warp_sums[32][kN];
   __shared__ int carry_s[kN];
+  __shared__ float red_f[32][3];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid < kN) carry_s[tid] = 0;
+  // this thread's share of the cost model: prefill SM-microseconds, the longest prefill item,
+  // split-KV bytes
+  float pf_us = 0.f, pf_long = 0.f, dec_bytes = 0.f;
   __syncthreads();
   for (int base = 0; base < p.num_seqs; base += 1024) {
     const int s = base + tid;
@@ -137,7 +143,26 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
       cnt[0] = decode_items_of(p, n, L, &bad);
       if (bad) set_error(&p.hdr->error, PA_DEVERR_LENGTHS);
       cnt[1] = prefill_items_of(p, n, L);
-      cnt[2] = (cnt[0] > 0 && partitions_of(p, L) > 1) ? n * p.num_q_heads : 0;
+      // rows the merge combines: split-KV sequences of two or more partitions, and prefill
+      // runs whose tiles are split along the keys
+      cnt[2] = ((cnt[0] > 0 && partitions_of(p, L) > 1) ||
+                (cnt[1] > 0 && prefill_splits(n, L, p.group, p.pmax) > 1))
+                   ? n * p.num_q_heads
+                   : 0;
+      if (cnt[0] > 0) dec_bytes += float(ceil_div(L, kBlockSize)) * p.num_kv_heads *
+                                   float(p.kv_tile_bytes);
+      if (cnt[1] > 0) {
+        // every prefill item of the sequence: its 128-key slices times the slice cost
+        const int tpt = 128 / p.group;
+        const int tiles = ceil_div(n, tpt);
+        const int ns = prefill_splits(n, L, p.group, p.pmax);
+        for (int t = 0; t < tiles; ++t) {
+          const int pos_last = L - n + min((t + 1) * tpt, n) - 1;
+          const float us = float(ceil_div(pos_last / 128 + 1, ns)) * kTileSliceUs + kTileItemUs;
+          pf_us += us * ns * p.num_kv_heads;
+          pf_long = fmaxf(pf_long, us);
+        }
+      }
     }
     int x[kN];  // inclusive warp scans
 #pragma unroll
@@ -182,12 +207,51 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
       for (int k = 0; k < kN; ++k) carry_s[k] = excl[k] + cnt[k];
     __syncthreads();
   }
+  // block reduction of the cost model
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    pf_us += __shfl_xor_sync(0xffffffffu, pf_us, o);
+    pf_long = fmaxf(pf_long, __shfl_xor_sync(0xffffffffu, pf_long, o));
+    dec_bytes += __shfl_xor_sync(0xffffffffu, dec_bytes, o);
+  }
+  if (lane == 0) {
+    red_f[warp][0] = pf_us;
+    red_f[warp][1] = pf_long;
+    red_f[warp][2] = dec_bytes;
+  }
+  __syncthreads();
   if (tid == 0) {
+    float w_pf = 0.f, longest = 0.f, bytes = 0.f;
+    for (int i = 0; i < 32; ++i) {
+      w_pf += red_f[i][0];
+      longest = fmaxf(longest, red_f[i][1]);
+      bytes += red_f[i][2];
+    }
+    // SMs for the prefill tiles: the P that minimises the later of the two kernels' ends,
+    // the prefill taking max(work / P, longest item) and the split-KV kernel streaming its
+    // bytes on the other SMs (capped by the chip's HBM rate)
+    const int items = carry_s[1];
+    const int pmax = max(1, min(p.sms, items));
+    int best_p = pmax;
+    if (bytes > 0.f && items > 0) {
+      float best = CUDART_INF_F;
+      for (int P = 1; P <= pmax; ++P) {
+        const float tp = fmaxf(w_pf / P, longest);
+        const float rate = fminf(kHbmBytesPerUs, float(p.sms - P) * kDecodeSmBytesPerUs);
+        const float td = rate > 0.f ? bytes / rate : CUDART_INF_F;
+        const float t = fmaxf(tp, td);
+        if (t < best * 0.999f) {
+          best = t;
+          best_p = P;
+        }
+      }
+    }
     p.item_start[p.num_seqs] = carry_s[0];
     p.pf_item_start[p.num_seqs] = carry_s[1];
     p.merge_start[p.num_seqs] = carry_s[2];
     p.hdr->decode_counter = 0;
     p.hdr->prefill_counter = 0;
+    p.hdr->pf_ctas = static_cast<uint32_t>(best_p);
   }
 }
 
@@ -251,8 +315,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (kFp8 && HPI > 1) ? 3 : 1)
     prefetch_tensormap(&vmap);
   }
   __syncthreads();
-  grid_dependency_wait();  // the plan (and everything before it on the stream) is complete
+  // Launched right after the plan, the kernel waits for it here.  Launched after the prefill
+  // tiles (which waited for the plan before letting this kernel launch), the plan is already
+  // complete: the kernel starts on the SMs the prefill left free and waits for the prefill
+  // only before it exits, so that whatever follows on the stream sees both done.
+  if (!p.wait_at_end) grid_dependency_wait();
+  if (p.span && threadIdx.x == 0) atomicMin(reinterpret_cast<unsigned long long*>(p.span),
+                                            static_cast<unsigned long long>(global_ns()));
 
+  // (the plan's arrays are complete before this grid launches in either case, and L1 holds
+  // nothing older than the launch, so plain loads read them)
   const int total_items = p.item_start[p.num_seqs];
   uint32_t it = 0;          // blocks this warp has consumed so far (stage / phase tracking)
   bool timed_out = false;
@@ -275,10 +347,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (kFp8 && HPI > 1) ? 3 : 1)
       const int n = p.qsl[s + 1] - t0;
       const int L = p.context_lens[s];
       const int tpt = R / (p.group * HPI);
+      const int istart = p.item_start[s];
       const int qtiles = ceil_div(n, tpt);
       const int nblk = ceil_div(L, kBlockSize);
       const int nparts = ceil_div(nblk, p.pblk);
-      int local = item - p.item_start[s];
+      int local = item - istart;
       const int part = local % nparts;
       local /= nparts;
       const int qt = local % qtiles;
@@ -686,6 +759,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (kFp8 && HPI > 1) ? 3 : 1)
     fence_proxy_async_smem();  // generic accesses to the stage buffers before the next TMA
     cur ^= 1;
   }
+  if (p.span && threadIdx.x == 0)
+    atomicMax(reinterpret_cast<unsigned long long*>(p.span) + 1,
+              static_cast<unsigned long long>(global_ns()));
+  if (p.wait_at_end) grid_dependency_wait();  // the prefill tiles of the step are complete
 }
 
 // Eight loads of kPer consecutive floats each, issued back to back in one asm block (so that
@@ -818,8 +895,13 @@ __global__ void __launch_bounds__(256, 2) merge_kernel(const DecodeParams p) {
     const int start = lane < span ? p.merge_start[lo + lane] : INT_MAX;
     const int s = lo + 31 - __clz(__ballot_sync(0xffffffffu, start <= c));
     const int local = c - p.merge_start[s];
-    const int64_t rid = static_cast<int64_t>(p.qsl[s]) * p.num_q_heads + local;
-    merge_row<D>(p, rid, partitions_of(p, p.context_lens[s]), lane);
+    const int t0 = p.qsl[s];
+    const int n = p.qsl[s + 1] - t0, L = p.context_lens[s];
+    const int64_t rid = static_cast<int64_t>(t0) * p.num_q_heads + local;
+    bool bad;
+    const int nparts = decode_items_of(p, n, L, &bad) > 0 ? partitions_of(p, L)
+                                                         : prefill_splits(n, L, p.group, p.pmax);
+    merge_row<D>(p, rid, nparts, lane);
   }
 }
 
@@ -910,7 +992,6 @@ cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const PoolMa
   p.pmax = ws.pmax;
   const bool prefill = use_prefill && prefill_path_enabled(a.cache, a.num_q_heads,
                                                           a.num_kv_heads);
-  p.pf_pairs = prefill && prefill_uses_pairs(a.max_query_len, p.group) ? 1 : 0;
   p.decode_max_query = prefill ? kDecodeMaxQuery : INT32_MAX;
   p.decode_max_rows = prefill ? kDecodeMaxRows : INT32_MAX;
   p.out_bf16 = a.out_dtype == PA_BF16;
@@ -929,22 +1010,25 @@ cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const PoolMa
   const bool rt2 = p.group > 8 || (!mixed && static_cast<int64_t>(dec_q) * p.group > 8);
   p.rows_per_tile = rt2 ? 16 : 8;
 
-  cudaError_t e = launch_dependent(plan_kernel, dim3(1), dim3(1024), 0, a.stream, p);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p.sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  p.kv_tile_bytes = 2 * kBlockSize * a.head_dim * (fp8 ? 1 : 2);
+  p.span = a.span;
+
+  e = launch_dependent(plan_kernel, dim3(1), dim3(1024), 0, a.stream, p);
   if (e != cudaSuccess) return e;
   // The prefill tiles (tensor pipe, key slices mostly from L2) and the split-KV decode (HBM)
-  // run side by side: the prefill kernel goes to a high-priority side stream forked from the
-  // caller's stream after the plan, so its CTAs are placed first and decode CTAs fill the SMs
-  // it leaves; the caller's stream joins it before returning.  Both paths only read what the
-  // plan wrote and write disjoint output rows.
-  SideStream side{};
+  // share the GPU, one stream, each kernel launched early (programmatic dependent launch):
+  // the prefill kernel waits for the plan, which has given it part of the SMs, and then lets
+  // the split-KV kernel launch; its CTAs fill the SMs the prefill left free at once (and the
+  // others as prefill CTAs end), and wait for the prefill kernel only before they exit.  Both
+  // only read what the plan and the append wrote, and write disjoint output rows.
   if (prefill) {
-    if ((e = side_stream(&side)) != cudaSuccess) return e;
-    if ((e = cudaEventRecord(side.fork, a.stream)) != cudaSuccess) return e;
-    if ((e = cudaStreamWaitEvent(side.stream, side.fork, 0)) != cudaSuccess) return e;
-    AttnArgs b = a;
-    b.stream = side.stream;
-    if ((e = launch_prefill(b, p.pf_item_start, p.hdr, maps)) != cudaSuccess) return e;
-    if ((e = cudaEventRecord(side.join, side.stream)) != cudaSuccess) return e;
+    PrefillScratch scratch{p.part_lse, p.part_o, p.pmax};
+    if ((e = launch_prefill(a, p.pf_item_start, p.hdr, maps, scratch)) != cudaSuccess) return e;
+    p.wait_at_end = 1;
   }
   if (fp8 && hpi == 2)
     e = run_decode<128, true, 2, 1, 2>(a, ws, p, kmap, vmap, before, after);
@@ -957,10 +1041,6 @@ cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const PoolMa
   else
     e = rt2 ? run_decode<64, false, 4, 2>(a, ws, p, kmap, vmap, before, after)
             : run_decode<64, false, 4, 1>(a, ws, p, kmap, vmap, before, after);
-  if (prefill) {
-    const cudaError_t j = cudaStreamWaitEvent(a.stream, side.join, 0);  // join even on error
-    if (e == cudaSuccess) e = j;
-  }
   return e;
 }
 

@@ -14,13 +14,29 @@ namespace pa {
 
 // ---------------------------------------------------------------------------------------------
 // Workspace header: word 0 = device error bits, word 1 = decode work counter,
-// word 2 = prefill work counter.
+// word 2 = prefill work counter, word 3 = CTAs (SMs) the plan gives the prefill tiles.
 // ---------------------------------------------------------------------------------------------
 struct WsHeader {
   uint32_t error;
   uint32_t decode_counter;
   uint32_t prefill_counter;
+  uint32_t pf_ctas;
 };
+
+// Plan-time cost model of a step whose prefill tiles and split-KV decode share the GPU, used to
+// split the SMs between them (tuning constants, measured on GB300): the time one SM spends on
+// one 128-key slice of a 128-row prefill tile and the fixed time of one item (its first copies
+// and MMAs, and its output); the HBM bytes per microsecond one SM's split-KV CTAs stream; and
+// the chip's HBM bytes per microsecond.
+constexpr float kTileSliceUs = 1.7f;
+constexpr float kTileItemUs = 9.0f;
+constexpr float kDecodeSmBytesPerUs = 7.5e4f;
+constexpr float kHbmBytesPerUs = 6.7e6f;
+
+// A load that bypasses L1: for values another kernel of the stream wrote before this kernel
+// was launched, read without a dependency wait in between.
+__device__ __forceinline__ int ld_cg(const int* p) { return __ldcg(p); }
+__device__ __forceinline__ uint32_t ld_cg(const uint32_t* p) { return __ldcg(p); }
 
 constexpr int kBlockSize = 16;            // tokens per physical block
 constexpr int kDecodeWarps = 4;           // warps per decode CTA
@@ -36,6 +52,25 @@ __host__ __device__ constexpr bool routes_to_prefill(int n, int G) {
   return n > kDecodeMaxQuery || n * G > kDecodeMaxRows;
 }
 constexpr float kLazyRescaleLog2 = 8.f;  // softmax base moves only past 2^8 growth
+
+// Key splits of the items of a query run on the prefill tiles.  A 128-row tile whose keys
+// span many 128-key slices would make one item set the kernel's critical path (the 512-token
+// chunk after a 2,048-token prefix: about 20 slices per tile), so every tile of such a run is
+// cut along the keys into ns items of about equal length, each writing a normalised partial
+// and its log-sum-exp; the last of them to finish merges.  A run splits when even its first
+// tile spans at least kSplitSlices slices per split, into at most kMaxSplits items, and only
+// when the workspace holds that many partials per row (pmax).
+constexpr int kSplitSlices = 24;
+constexpr int kMaxSplits = 4;
+__host__ __device__ inline int prefill_splits(int n, int L, int G, int pmax) {
+  const int tpt = 128 / G;
+  const int first = tpt < n ? tpt : n;
+  const int slices = (L - n + first - 1) / 128 + 1;  // of the first tile
+  int ns = slices / kSplitSlices;
+  if (ns > kMaxSplits) ns = kMaxSplits;
+  if (ns > pmax) ns = pmax;
+  return ns < 1 ? 1 : ns;
+}
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // default limit of a bounded wait
 
 __device__ __forceinline__ void set_error(uint32_t* err, uint32_t bits) {

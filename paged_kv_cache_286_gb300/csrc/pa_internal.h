@@ -53,6 +53,7 @@ struct AttnArgs {
   cudaStream_t stream;
   cudaEvent_t pf_before = nullptr;  // benchmark hook: recorded around the prefill kernel
   cudaEvent_t pf_after = nullptr;
+  uint64_t* span = nullptr;         // benchmark hook: kernel start / end times (pa.h)
   uint64_t wait_ns = 0;             // limit of every bounded device-side wait
   int32_t skip_copy = 0;            // test hook (pa_test_skip_one_copy)
 };
@@ -149,17 +150,19 @@ struct PrefillParams {
   float score_log2;
   uint64_t wait_ns;   // limit of every bounded wait
   int32_t skip_copy;  // test hook: the first item claimed leaves out its first K copy
+  uint64_t* span;     // benchmark hook: [first CTA start, last CTA end] in ns, or NULL
+  float* part_lse;       // [T][Hq][pmax] log2-domain log-sum-exp of split partials
+  float* part_o;         // [T][Hq][pmax][128] normalised split partials
+  int32_t pmax;          // partials per row the workspace holds (>= the splits of a pair)
 };
 
-// A high-priority stream of the current device for the prefill-tile kernel, and two events of
-// the calling thread to fork it from and join it to the caller's stream.  Created on first use
-// (per device; the events per thread and device) and kept for the life of the process.
-struct SideStream {
-  cudaStream_t stream;
-  cudaEvent_t fork;
-  cudaEvent_t join;
+// Where split prefill tiles keep their partials (the workspace's split-KV arrays).
+struct PrefillScratch {
+  float* part_lse;
+  float* part_o;
+  int32_t pmax;
 };
-cudaError_t side_stream(SideStream* out);
+
 
 // Tensor maps of one call: the pool as 2-D rows (split-KV kernel, verify tiles), the pool as
 // 4-D whole (block, kv head) tiles and q as 3-D tiles (prefill kernels; NULL when unused).
@@ -168,15 +171,14 @@ struct PoolMaps {
   bool has_k4 = false, has_q3 = false;
 };
 
-// Whether the step's prefill runs take the two-tile chunk kernel (runs of more than 64 rows)
-// rather than the one-tile verify kernel with rows split over two warps.
-inline bool prefill_uses_pairs(int32_t max_query_len, int32_t group) {
-  return static_cast<int64_t>(max_query_len) * group > 64;
+// Whether the step's prefill tiles take the kernel instance with each row split over two
+// softmax warps: when every run has at most 64 (token x head) rows, as in speculative verify.
+inline bool prefill_rows_split(int32_t max_query_len, int32_t group) {
+  return static_cast<int64_t>(max_query_len) * group <= 64;
 }
 
 cudaError_t launch_prefill(const AttnArgs& a, const int32_t* item_start, WsHeader* hdr,
-                           const PoolMaps& maps);
-cudaError_t launch_chunk(const AttnArgs& a, const PrefillParams& p, const CUtensorMap& qmap,
-                         const CUtensorMap& kmap4, const CUtensorMap& vmap4);
+                           const PoolMaps& maps, const PrefillScratch& scratch);
+
 
 }  // namespace pa

@@ -9,36 +9,52 @@
 // more than 16 (token x head) rows comes here.
 //
 // Design (GB300 / sm_103a; bf16 K/V, head_dim 128):
-//  * One work item = (sequence, kv head, tile of 128 rows), a row being (query token, q head of
-//    the GQA group), so the tile's queries share every K/V tile they read.  Items are taken
-//    longest-first from an atomic counter by persistent CTAs (one per SM).
-//  * Warp 0 issues TMA copies of the q tile once (a 3-D box of tokens x heads x 64 columns, two
-//    boxes), then for every 128 keys the 8 (block, kv head) K tiles of the block table; warp 6
-//    does the same for the V tiles.  Eight lanes of each issue one block's boxes apiece, into
-//    three-stage K and V rings (128-byte swizzle, completion on mbarriers).
+//  * A tile is 128 rows, a row being (query token, q head of the GQA group), so the tile's
+//    queries share every K/V tile they read.  One work item is a tile over a range of 128-key
+//    slices: the tiles of very long runs are cut along the keys into several items
+//    (prefill_splits), each writing a normalised partial and its log-sum-exp into the
+//    workspace's split-KV arrays, which the merge kernel combines like the split-KV
+//    partitions.  Persistent CTAs (one per SM, as many as the plan gives this kernel) take
+//    items longest-first from an atomic counter; the V producer claims the CTA's next item while
+//    the current one runs.
+//  * The pool is viewed by a 4-D tensor map as (64 columns, 8 rows, 2 column halves, 8-row
+//    groups), so that one TMA copy brings a whole 16 x 128 (block, kv head) tile: 8 copies per
+//    128 keys for K (lanes of warp 0, which also loads the q tile) and 8 for V (warp 6), into
+//    three-stage rings.  One SM's TMA unit is limited by the number of copies rather than their
+//    bytes, so whole-tile copies halve the copy time of a slice.  In shared memory a block's
+//    tile is [2 row groups][2 halves][8 rows][128 bytes] with the 128-byte swizzle, i.e. 8-key
+//    groups 2 KiB apart and the column halves 1 KiB apart, which the MMA descriptors express
+//    as strides.
 //  * Warp 1 issues tcgen05.mma from one thread: S = Q K^T into one of three TMEM buffers
 //    (128 x 128 fp32), and O += P V into a fourth, with P read from TMEM and V from shared
-//    memory (MN-major).  The softmax threads write P back over their S columns as bf16 hi and
-//    lo parts (keys 0-63: hi in columns 0-31, lo in 32-63; keys 64-127 likewise in 64-127), so
-//    P V is exact to ~2^-16 like the decode path, and the next tile's softmax can run while
-//    this tile's P V is in flight.
+//    memory (MN-major).  S of the next two slices is computed while the softmax works on the
+//    current one.  The softmax threads write P back over their S columns as bf16 hi and lo
+//    parts (keys 0-63: hi in columns 0-31, lo in 32-63; keys 64-127 likewise in 64-127), so
+//    P V is exact to ~2^-16 like the decode path.
 //  * Softmax, one thread per row (TMEM lane): it reads its row of S from TMEM once, masks keys
-//    beyond the row's position, keeps the running max in the log2 domain and rescales O in
-//    TMEM only when the max grows by more than 2^8 (the final division uses the same max, so
-//    the result is exact), and finally divides O by the row sum and stores it.  Warps 2-5 do
-//    this for whole rows.  When every run has at most 64 rows (speculative verify), at most
-//    two of the four lane quarters hold rows, and the kernel instance with the row split runs
-//    instead: warps 2-5 take keys (and O columns) 0-63 and warps 7-10 keys 64-127, the two
-//    threads of a row agreeing on its max, and at the end adding their sums, through a
-//    shared-memory slot and an mbarrier of the pair.  A warp can only reach the lane quarter
-//    of its own SM sub-partition, so the split puts a second warp on each busy sub-partition
-//    to hide the latency of the exponentials and TMEM traffic.
+//    beyond the row's position, keeps the running max in the log2 domain (set by the first
+//    slice that shows the row a key) and rescales O in TMEM only when the max grows by more
+//    than 2^8 (the final division uses the same max, so the result is exact), and finally
+//    divides O by the row sum.  Warps 2-5 do this for whole rows.  When every run has at most
+//    64 rows (speculative verify), at most two of the four lane quarters hold rows, and the
+//    kernel instance with the row split runs instead: warps 2-5 take keys (and O columns)
+//    0-63 and warps 7-10 keys 64-127, the two threads of a row agreeing on its max, and at the
+//    end adding their sums, through a shared-memory slot and an mbarrier of the pair.  A warp
+//    can only reach the lane quarter of its own SM sub-partition, so the split puts a second
+//    warp on each busy sub-partition to hide the latency of the exponentials and TMEM traffic.
 //  * V rows past the last valid key (stale slots, possibly NaN) are zeroed in shared memory
 //    before P V reads them; K there only feeds masked scores.
+//  * The epilogue stages each warp's rows in the idle K stages (swizzled) and writes whole
+//    rows per instruction, instead of one scattered 16-byte piece per row and instruction.
+//  * Launched right after the plan (programmatic dependent launch): the CTAs beyond the SMs
+//    the plan gives this kernel end at once, and the split-KV kernel launches onto the rest.
+//  * Every wait is bounded; on expiry the CTA records PA_DEVERR_TIMEOUT, stops, lets the copies
+//    and MMAs it issued finish (bounded waits again) and frees its tensor memory.
 #include <math_constants.h>
 
 #include <algorithm>
 #include <climits>
+#include <type_traits>
 
 #include "pa_common.cuh"
 #include "pa_internal.h"
@@ -50,11 +66,12 @@ constexpr int kRows = 128;
 constexpr int kKeys = 128;
 constexpr int kStages = 3;   // K and V ring depth
 constexpr int kSBufs = 3;    // S/P buffers in TMEM (3 x 128 columns) ahead of O
-constexpr int kHalf = 16384;  // one 64-column region of a 128-row bf16 tile
+constexpr int kHalf = 16384;  // one 64-column half of the q tile
 constexpr int kTile = 32768;  // 128 x 128 bf16
+constexpr int kBlockBytes = 4096;  // one (block, kv head) tile of a K or V stage
 constexpr int kQ = 0, kK = kTile, kV = kK + kStages * kTile;
-constexpr int kCtl = kV + kStages * kTile;  // control block (barriers, item, flags)
-constexpr int kXBar = kCtl + 256;           // 4 mbarriers: one per pair of softmax warps
+constexpr int kCtl = kV + kStages * kTile;  // control block (barriers, items, flags)
+constexpr int kXBar = kCtl + 384;           // 4 mbarriers: one per pair of softmax warps
 constexpr int kXSlot = kXBar + 32;          // 3 x 128 row slots of the pairs' exchanges
 constexpr int kXBufs = 3;
 constexpr int kVWarp = 6;     // V producer (warp 0 loads q and K)
@@ -64,28 +81,29 @@ constexpr int kVWarp = 6;     // V producer (warp 0 loads q and K)
 __host__ __device__ constexpr int threads(bool split) { return split ? 352 : 224; }
 __host__ __device__ constexpr int softmax_threads(bool split) { return split ? 256 : 128; }
 __host__ __device__ constexpr int smem_bytes(bool split) {
-  return 1024 + (split ? kXSlot + kXBufs * kRows * 4 : kCtl + 256);
+  return 1024 + (split ? kXSlot + kXBufs * kRows * 4 : kCtl + 384);
 }
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = kSBufs * 128;
 constexpr float kRescaleLog2 = 8.f;
 }  // namespace pf
 
-
 struct PfItem {
-  int s, h, t0, ntok, pos0, L, nkv, nblk_tile, valid, first;
+  int s, h, t0, ntok, pos0, L, nblk_tile, valid, first;
+  int j0, nj;       // the item's slices of the tile: j0 .. j0 + nj - 1
+  int ns, k;        // splits of the tile and this item's split
 };
 
 struct PfCtl {
   uint64_t q_full, k_full[pf::kStages], k_empty[pf::kStages], v_full[pf::kStages],
-      v_empty[pf::kStages], s_full[pf::kSBufs], p_full[pf::kSBufs], o_done[pf::kSBufs];
+      v_empty[pf::kStages], s_full[pf::kSBufs], p_full[pf::kSBufs], o_done[pf::kSBufs], drain;
   uint32_t tmem_base;
   int abort_flag;
   int v_zero_from[pf::kStages];
   uint32_t v_bad[pf::kStages];
-  PfItem item;
+  PfItem item[2];  // the current item and the next one, by the parity of the item count
 };
-static_assert(sizeof(PfCtl) <= 256, "control block too large");
+static_assert(sizeof(PfCtl) <= 384, "control block too large");
 static_assert(pf::smem_bytes(true) <= 232448, "more shared memory than a CTA may have");
 
 // Floats mapped to ints of the same order (an involution), so that integer atomicMax takes the
@@ -98,6 +116,50 @@ __device__ __forceinline__ float order_key_float(int k) {
   return __int_as_float(k >= 0 ? k : (k ^ 0x7fffffff));
 }
 
+// Claims the next item from the counter (longest items, the last tiles of the last runs,
+// first) and decodes it.
+__device__ __forceinline__ PfItem claim_item(const PrefillParams& p, int total) {
+  PfItem it;
+  const int rev = static_cast<int>(atomicAdd(&p.hdr->prefill_counter, 1u));
+  const int item = total - 1 - rev;
+  it.valid = item >= 0;
+  it.first = rev == 0;
+  if (!it.valid) return it;
+  int lo = 0, hi = p.num_seqs;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (p.item_start[mid] <= item) lo = mid; else hi = mid;
+  }
+  const int s = lo;
+  const int t0 = p.qsl[s];
+  const int n = p.qsl[s + 1] - t0;
+  const int L = p.context_lens[s];
+  const int tpt = pf::kRows / p.group;
+  const int qtiles = (n + tpt - 1) / tpt;
+  const int ns = prefill_splits(n, L, p.group, p.pmax);
+  const int local = item - p.item_start[s];
+  const int k = local % ns;
+  const int ti = local / ns;
+  const int h = ti / qtiles;
+  const int qt = ti - h * qtiles;
+  const int i0 = qt * tpt;
+  it.s = s;
+  it.h = h;
+  it.t0 = t0 + i0;
+  it.ntok = min(tpt, n - i0);
+  it.pos0 = L - n + i0;
+  it.L = L;
+  it.ns = ns;
+  it.k = k;
+  const int pmax = it.pos0 + it.ntok - 1;
+  const int nkv = pmax / pf::kKeys + 1;  // slices of the tile
+  const int per = (nkv + ns - 1) / ns;
+  it.j0 = min(nkv, k * per);
+  it.nj = min(nkv, it.j0 + per) - it.j0;
+  it.nblk_tile = pmax / kBlockSize + 1;
+  return it;
+}
+
 template <bool kSplit>
 __global__ void __launch_bounds__(pf::threads(kSplit), 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap,
@@ -108,6 +170,15 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   PfCtl* ctl = reinterpret_cast<PfCtl*>(smem + pf::kCtl);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Launched right after the plan (programmatic dependent launch): wait for its items and SM
+  // budget, let the split-KV kernel launch onto the SMs this kernel leaves, and end the CTAs
+  // beyond the budget at once.
+  grid_dependency_wait();
+  grid_launch_dependents();
+  if (blockIdx.x >= ld_cg(&p.hdr->pf_ctas)) return;
+  if (p.span && threadIdx.x == 0) atomicMin(reinterpret_cast<unsigned long long*>(p.span),
+                                            static_cast<unsigned long long>(global_ns()));
+  const int total = p.item_start[p.num_seqs];
 
   if (tid == 0) {
     mbar_init(&ctl->q_full, 1);
@@ -124,6 +195,7 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
       mbar_init(&ctl->p_full[i], pf::softmax_threads(kSplit));
       mbar_init(&ctl->o_done[i], 1);
     }
+    mbar_init(&ctl->drain, 1);
     if (kSplit)
       for (int q = 0; q < 4; ++q)
         mbar_init(reinterpret_cast<uint64_t*>(smem + pf::kXBar) + q, 2);  // one lane a warp
@@ -132,6 +204,7 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
     prefetch_tensormap(&qmap);
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
+    ctl->item[0] = claim_item(p, total);
   }
   int* xslot = reinterpret_cast<int*>(smem + pf::kXSlot);  // [kXBufs][kRows], split only
   if (kSplit)
@@ -141,12 +214,11 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
-  const int total = p.item_start[p.num_seqs];
-  uint32_t tc = 0;  // KV tiles processed by this CTA so far (ring / phase tracking)
+  uint32_t tc = 0;  // KV slices processed by this CTA so far (ring / phase tracking)
   uint32_t ic = 0;  // items processed by this CTA so far
   uint32_t xc = 0;  // exchanges of this softmax thread's pair so far (slot / phase tracking)
+  uint32_t kiss = 0, viss = 0, qiss = 0;  // producers: K, V and q fills issued (final drain)
   const int G = p.group;
-  const int tpt = pf::kRows / G;  // query tokens per tile
 
   auto fail = [&](uint32_t bits) {
     set_error(&p.hdr->error, bits);
@@ -160,52 +232,20 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
   };
 
   while (true) {
-    if (tid == 0) {
-      PfItem it;
-      const int rev = static_cast<int>(atomicAdd(&p.hdr->prefill_counter, 1u));
-      const int item = total - 1 - rev;  // longest items (last tiles of a chunk) first
-      it.valid = item >= 0;
-      it.first = rev == 0;
-      if (it.valid) {
-        int lo = 0, hi = p.num_seqs;
-        while (hi - lo > 1) {
-          const int mid = (lo + hi) >> 1;
-          if (p.item_start[mid] <= item) lo = mid; else hi = mid;
-        }
-        const int s = lo;
-        const int t0 = p.qsl[s];
-        const int n = p.qsl[s + 1] - t0;
-        const int L = p.context_lens[s];
-        const int qtiles = (n + tpt - 1) / tpt;
-        const int local = item - p.item_start[s];
-        const int h = local / qtiles;
-        const int qt = local - h * qtiles;
-        const int i0 = qt * tpt;
-        it.s = s;
-        it.h = h;
-        it.t0 = t0 + i0;
-        it.ntok = min(tpt, n - i0);
-        it.pos0 = L - n + i0;
-        it.L = L;
-        const int pmax = it.pos0 + it.ntok - 1;
-        it.nkv = pmax / pf::kKeys + 1;
-        it.nblk_tile = pmax / kBlockSize + 1;
-      }
-      ctl->item = it;
-    }
-    __syncthreads();
-    const PfItem I = ctl->item;
+    const PfItem I = ctl->item[ic & 1u];
     if (!I.valid || ctl->abort_flag) break;
 
     if (warp == 0 || warp == pf::kVWarp) {
       // ------------------------------------------------------- producers (TMA): warp 0 q and K,
       // warp 6 V.  Two issuing warps double the rate at which tile copies enter the TMA unit.
       const bool k_side = warp == 0;
+      if (!k_side && lane == 0) ctl->item[(ic + 1) & 1u] = claim_item(p, total);  // the next
       if (k_side && lane == 0) {
         mbar_arrive_expect_tx(&ctl->q_full, pf::kTile);
         tma_load_3d(smem + pf::kQ, &qmap, 0, I.h * G, I.t0, &ctl->q_full);
         tma_load_3d(smem + pf::kQ + pf::kHalf, &qmap, 64, I.h * G, I.t0, &ctl->q_full);
       }
+      if (k_side) ++qiss;
       // Block-table entries are read 32 at a time (lane l holds block 32 * grp + l) with the
       // next group prefetched, so no TMA issue waits on a dependent table load.
       const int32_t* trow = p.block_tables + static_cast<int64_t>(I.s) * p.max_blocks_per_seq;
@@ -213,20 +253,23 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
         const int jb = 32 * grp + lane;
         return jb < I.nblk_tile ? __ldg(trow + jb) : -1;
       };
-      int grp_cur = 0;
-      int tab_cur = tab_load(0);
-      int tab_next = tab_load(1);
-      // block ids of slice j for lanes 0-7 (-1 = not loaded), plus masks of loadable / bad ones
-      auto slice = [&](int j, int& phys, uint32_t& ok_mask, uint32_t& bad_mask) {
+      int grp_cur = I.j0 >> 2;
+      int tab_cur = tab_load(grp_cur);
+      int tab_next = tab_load(grp_cur + 1);
+      const int yrow0 = I.h * 2;  // 8-row group of (block 0, this kv head)
+      for (int jj = 0; jj < I.nj; ++jj) {
+        const int j = I.j0 + jj;
         const int grp = j >> 2;
         if (grp != grp_cur) {
           tab_cur = tab_next;
           tab_next = tab_load(grp + 1);
           grp_cur = grp;
         }
+        // block ids of slice j for lanes 0-7 (-1 = not loaded), plus masks of loadable / bad
+        // ones
         const int e = __shfl_sync(0xffffffffu, tab_cur, 8 * (j & 3) + (lane & 7));
         const int jb = 8 * j + lane;
-        phys = -1;
+        int phys = -1;
         bool bad = false;
         if (lane < 8 && jb < I.nblk_tile) {
           if (e < 0 || e >= p.num_blocks) {
@@ -236,72 +279,59 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
             phys = e;
           }
         }
-        ok_mask = __ballot_sync(0xffffffffu, phys >= 0);
-        bad_mask = __ballot_sync(0xffffffffu, bad);
-      };
-      auto load_k = [&](int j, int phys, uint32_t okm) -> bool {
-        const uint32_t g = tc + j, st = g % pf::kStages;
-        const uint32_t bytes = __popc(okm) * 2u * 2048u;
-        if (!wait(&ctl->k_empty[st], ((g / pf::kStages) & 1u) ^ 1u)) return false;
-        if (lane == 0) {
-          if (bytes) mbar_arrive_expect_tx(&ctl->k_full[st], bytes);
-          else mbar_arrive(&ctl->k_full[st]);
+        const uint32_t okm = __ballot_sync(0xffffffffu, phys >= 0);
+        const uint32_t badm = __ballot_sync(0xffffffffu, bad);
+        const uint32_t bytes = __popc(okm) * static_cast<uint32_t>(pf::kBlockBytes);
+        const int ycoord = (phys * p.num_kv_heads) * 2 + yrow0;
+        const uint32_t g = tc + jj, st = g % pf::kStages;
+        if (k_side) {
+          if (!wait(&ctl->k_empty[st], ((g / pf::kStages) & 1u) ^ 1u)) break;
+          if (lane == 0) {
+            if (bytes) mbar_arrive_expect_tx(&ctl->k_full[st], bytes);
+            else mbar_arrive(&ctl->k_full[st]);
+          }
+          __syncwarp();
+          // test hook: lane 0's copy of the first slice of the first item claimed is left
+          // out (its bytes are still expected), so that the bounded waits on that stage expire
+          const bool skip = p.skip_copy && I.first && jj == 0 && lane == 0;
+          if (phys >= 0 && !skip)
+            tma_load_4d(smem + pf::kK + st * pf::kTile + lane * pf::kBlockBytes, &kmap, 0, 0,
+                        0, ycoord, &ctl->k_full[st]);
+          ++kiss;
+        } else {
+          if (!wait(&ctl->v_empty[st], ((g / pf::kStages) & 1u) ^ 1u)) break;
+          if (lane == 0) {
+            // rows the MMA warp has to clear: keys past the last valid one, and bad blocks
+            const int valid_end = min(I.L, I.nblk_tile * kBlockSize) - j * pf::kKeys;
+            ctl->v_zero_from[st] = max(0, min(pf::kKeys, valid_end));
+            ctl->v_bad[st] = badm;
+            if (bytes) mbar_arrive_expect_tx(&ctl->v_full[st], bytes);
+            else mbar_arrive(&ctl->v_full[st]);
+          }
+          __syncwarp();
+          if (phys >= 0)
+            tma_load_4d(smem + pf::kV + st * pf::kTile + lane * pf::kBlockBytes, &vmap, 0, 0,
+                        0, ycoord, &ctl->v_full[st]);
+          ++viss;
         }
-        __syncwarp();
-        // test hook: lane 0's copy of the first slice of the first item claimed is left out
-        // (its bytes are still expected), so that the bounded waits on that stage expire
-        const bool skip = p.skip_copy && I.first && j == 0 && lane == 0;
-        if (phys >= 0 && !skip) {
-          const int yrow = (phys * p.num_kv_heads + I.h) * kBlockSize;
-          uint8_t* kt = smem + pf::kK + st * pf::kTile + lane * 2048;
-          tma_load_2d(kt, &kmap, 0, yrow, &ctl->k_full[st]);
-          tma_load_2d(kt + pf::kHalf, &kmap, 64, yrow, &ctl->k_full[st]);
-        }
-        return true;
-      };
-      auto load_v = [&](int j, int phys, uint32_t okm, uint32_t badm) -> bool {
-        const uint32_t g = tc + j, st = g % pf::kStages;
-        const uint32_t bytes = __popc(okm) * 2u * 2048u;
-        if (!wait(&ctl->v_empty[st], ((g / pf::kStages) & 1u) ^ 1u)) return false;
-        if (lane == 0) {
-          // rows the MMA warp has to clear: keys past the last valid one, and bad blocks
-          const int valid_end = min(I.L, I.nblk_tile * kBlockSize) - j * pf::kKeys;
-          ctl->v_zero_from[st] = max(0, min(pf::kKeys, valid_end));
-          ctl->v_bad[st] = badm;
-          if (bytes) mbar_arrive_expect_tx(&ctl->v_full[st], bytes);
-          else mbar_arrive(&ctl->v_full[st]);
-        }
-        __syncwarp();
-        if (phys >= 0) {
-          const int yrow = (phys * p.num_kv_heads + I.h) * kBlockSize;
-          uint8_t* vt = smem + pf::kV + st * pf::kTile + lane * 2048;
-          tma_load_2d(vt, &vmap, 0, yrow, &ctl->v_full[st]);
-          tma_load_2d(vt + pf::kHalf, &vmap, 64, yrow, &ctl->v_full[st]);
-        }
-        return true;
-      };
-      for (int j = 0; j < I.nkv; ++j) {
-        int ph;
-        uint32_t okm, badm;
-        slice(j, ph, okm, badm);
-        if (!(k_side ? load_k(j, ph, okm) : load_v(j, ph, okm, badm))) break;
       }
     } else if (warp == 1) {
       // ------------------------------------------------------------- MMA issuer ---------
       const uint32_t id_s = idesc_bf16_f32(128, 128, false);
       const uint32_t id_pv = idesc_bf16_f32(128, 128, true);
       const uint32_t q_addr = smem_u32(smem + pf::kQ);
-      auto issue_s = [&](int j) -> bool {
-        const uint32_t g = tc + j, st = g % pf::kStages, b = g % pf::kSBufs;
+      auto issue_s = [&](int jj) -> bool {
+        const uint32_t g = tc + jj, st = g % pf::kStages, b = g % pf::kSBufs;
         if (!wait(&ctl->k_full[st], (g / pf::kStages) & 1u)) return false;
         tc_fence_after();
         if (lane == 0) {
           const uint32_t k_addr = smem_u32(smem + pf::kK + st * pf::kTile);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t off = (ks >> 2) * pf::kHalf + (ks & 3) * 32;
-            tc_mma_bf16(tmem + b * 128u, smem_desc_sw128(q_addr + off, 16, 1024),
-                        smem_desc_sw128(k_addr + off, 16, 1024), id_s, ks > 0);
+            const uint32_t qa = q_addr + (ks >> 2) * pf::kHalf + (ks & 3) * 32;
+            const uint32_t kb = k_addr + (ks >> 2) * 1024 + (ks & 3) * 32;
+            tc_mma_bf16(tmem + b * 128u, smem_desc_sw128(qa, 16, 1024),
+                        smem_desc_sw128(kb, 16, 2048), id_s, ks > 0);
           }
           tc_commit(&ctl->s_full[b]);
           tc_commit(&ctl->k_empty[st]);
@@ -311,20 +341,21 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
       };
       bool ok = wait(&ctl->q_full, ic & 1u);
       if (ok) tc_fence_after();
-      for (int j = 0; ok && j < min(pf::kSBufs, I.nkv); ++j) ok = issue_s(j);
-      for (int j = 0; ok && j < I.nkv; ++j) {
-        const uint32_t g = tc + j, st = g % pf::kStages, b = g % pf::kSBufs;
+      for (int jj = 0; ok && jj < min(pf::kSBufs, I.nj); ++jj) ok = issue_s(jj);
+      for (int jj = 0; ok && jj < I.nj; ++jj) {
+        const uint32_t g = tc + jj, st = g % pf::kStages, b = g % pf::kSBufs;
         if (!(ok = wait(&ctl->v_full[st], (g / pf::kStages) & 1u))) break;
         uint8_t* vt = smem + pf::kV + st * pf::kTile;
         const int zf = ctl->v_zero_from[st];
         const uint32_t badm = ctl->v_bad[st];
         if (zf < pf::kKeys || badm) {
-          // clear the 128-byte rows (both column halves) of keys that hold no valid value
+          // clear the 128-byte rows (both column halves) of keys that hold no valid value;
+          // key kk of the slice: block kk / 16, row group (kk / 8) % 2, row kk % 8
           for (int e = lane; e < pf::kKeys * 2 * 8; e += 32) {
             const int key = e >> 4, half = (e >> 3) & 1, c16 = e & 7;
             if (key >= zf || ((badm >> (key >> 4)) & 1u))
-              *reinterpret_cast<uint4*>(vt + half * pf::kHalf + key * 128 + c16 * 16) =
-                  make_uint4(0u, 0u, 0u, 0u);
+              *reinterpret_cast<uint4*>(vt + (key >> 3) * 2048 + half * 1024 + (key & 7) * 128 +
+                                        c16 * 16) = make_uint4(0u, 0u, 0u, 0u);
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -334,24 +365,26 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
         if (lane == 0) {
           const uint32_t v_addr = smem_u32(vt);
           // P of keys 16 ks .. 16 ks + 15: the hi parts of keys 0-63 in columns 0-31 of the
-          // buffer and their lo parts in 32-63; keys 64-127 the same in columns 64-127
+          // buffer and their lo parts in 32-63; keys 64-127 the same in columns 64-127.  V of
+          // those keys: block ks of the stage, MN-major (the column halves 1 KiB apart, 8-key
+          // groups 2 KiB apart).
           auto p_col = [&](int ks) { return tmem + b * 128u + (ks >> 2) * 64u + (ks & 3) * 8u; };
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
             tc_mma_bf16_ts(tmem + pf::kOCol, p_col(ks),
-                           smem_desc_sw128(v_addr + ks * 2048, pf::kHalf, 1024), id_pv,
-                           j > 0 || ks > 0);
+                           smem_desc_sw128(v_addr + ks * 4096, 1024, 2048), id_pv,
+                           jj > 0 || ks > 0);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
             tc_mma_bf16_ts(tmem + pf::kOCol, p_col(ks) + 32u,
-                           smem_desc_sw128(v_addr + ks * 2048, pf::kHalf, 1024), id_pv, true);
+                           smem_desc_sw128(v_addr + ks * 4096, 1024, 2048), id_pv, true);
           tc_commit(&ctl->o_done[b]);
           tc_commit(&ctl->v_empty[st]);
         }
         __syncwarp();
-        // S of tile j+3 reuses this tile's S/P buffer: it is issued after (and runs after) the
-        // P V that reads P from it
-        if (j + pf::kSBufs < I.nkv) ok = issue_s(j + pf::kSBufs);
+        // S of slice jj+3 reuses this slice's S/P buffer: it is issued after (and runs after)
+        // the P V that reads P from it
+        if (jj + pf::kSBufs < I.nj) ok = issue_s(jj + pf::kSBufs);
       }
     } else {
       // ------------------------------------------------------------- softmax rows -------
@@ -390,9 +423,10 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
       // a pair see the same rows)
       const bool live = __any_sync(0xffffffffu, row_ok);
       float m_used = 0.f, l = 0.f;
+      bool seen = false;  // whether m_used comes from a visible key yet
       bool ok = true;
-      for (int j = 0; j < I.nkv; ++j) {
-        const uint32_t g = tc + j, b = g % pf::kSBufs;
+      for (int jj = 0; jj < I.nj; ++jj) {
+        const uint32_t g = tc + jj, b = g % pf::kSBufs;
         if (!(ok = wait(&ctl->s_full[b], (g / pf::kSBufs) & 1u))) break;
         tc_fence_after();
         const uint32_t sb = tl + b * 128u + hc;  // this thread's columns of S, then of P
@@ -408,14 +442,15 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
           continue;
         }
         // keys 0..kmax of this thread's columns are visible
-        const int kmax = row_ok ? row_pos - j * pf::kKeys - half * 64 : -1;
+        const int kmax = row_ok ? row_pos - (I.j0 + jj) * pf::kKeys - half * 64 : -1;
         uint32_t sv[kC];
 #pragma unroll
         for (int c = 0; c < kC / 32; ++c)
           tmem_ld32(sb + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
         tmem_wait_ld();
-        // scores in the log2 domain; masked keys become -inf.  Eight independent max / sum
-        // accumulators keep the dependency chains short.
+        // raw scores, masked keys -inf; the row max is taken on them (the scale is positive)
+        // and moved to the log2 domain once.  Eight independent max / sum accumulators keep
+        // the dependency chains short.
         float x[kC];
         float mx[8];
 #pragma unroll
@@ -423,13 +458,13 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
         if (__all_sync(0xffffffffu, kmax >= kC - 1)) {  // warp-uniform branch
 #pragma unroll
           for (int i = 0; i < kC; ++i) {
-            x[i] = __uint_as_float(sv[i]) * p.score_log2;
+            x[i] = __uint_as_float(sv[i]);
             mx[i & 7] = fmaxf(mx[i & 7], x[i]);
           }
         } else {
 #pragma unroll
           for (int i = 0; i < kC; ++i) {
-            x[i] = (i <= kmax) ? __uint_as_float(sv[i]) * p.score_log2 : -CUDART_INF_F;
+            x[i] = (i <= kmax) ? __uint_as_float(sv[i]) : -CUDART_INF_F;
             mx[i & 7] = fmaxf(mx[i & 7], x[i]);
           }
         }
@@ -438,17 +473,24 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))),
                             false, &mt)))
           break;
+        if (mt != -CUDART_INF_F) mt *= p.score_log2;
         bool rescale = false;
         float m_new = m_used;
-        if (j == 0) {
-          m_new = (mt == -CUDART_INF_F) ? 0.f : mt;
+        if (!seen) {
+          // O and l of the row are still zero: the first visible key sets the base
+          if (mt != -CUDART_INF_F) {
+            m_new = mt;
+            seen = true;
+          }
         } else if (mt > m_used + pf::kRescaleLog2) {
           m_new = mt;
           rescale = true;
         }
         const float alpha = rescale ? fast_exp2(m_used - m_new) : 1.f;
-        // probabilities; for every 64 keys, bf16 hi parts into their columns 0..31 and lo
-        // parts into 32..63
+        // probabilities 2^(s * scale * log2 e - m); for every 64 keys, bf16 hi parts into their
+        // columns 0..31 and lo parts into 32..63.  The split is by truncation, on the integer
+        // pipes: hi keeps the upper 16 bits of p, lo = p - hi exactly in fp32, and lo is
+        // truncated in turn, so hi + lo = p within 2^-14 relative.
         float rsum[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) rsum[i] = 0.f;
@@ -457,11 +499,14 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
           uint32_t hi[16], lo[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float p0 = fast_exp2(x[c * 32 + 2 * e] - m_new);
-            const float p1 = fast_exp2(x[c * 32 + 2 * e + 1] - m_new);
+            const float p0 = fast_exp2(fmaf(x[c * 32 + 2 * e], p.score_log2, -m_new));
+            const float p1 = fast_exp2(fmaf(x[c * 32 + 2 * e + 1], p.score_log2, -m_new));
             rsum[e & 7] += p0 + p1;
-            hi[e] = pack_bf16x2(p0, p1);
-            lo[e] = pack_bf16x2(p0 - bf16lo_to_f32(hi[e]), p1 - bf16hi_to_f32(hi[e]));
+            const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+            hi[e] = prmt(b0, b1, 0x7632u);
+            const float l0 = p0 - __uint_as_float(b0 & 0xffff0000u);
+            const float l1 = p1 - __uint_as_float(b1 & 0xffff0000u);
+            lo[e] = prmt(__float_as_uint(l0), __float_as_uint(l1), 0x7632u);
           }
           const uint32_t pc = sb + (c >> 1) * 64 + (c & 1) * 16;
           tmem_st16(pc, hi);
@@ -472,7 +517,7 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
         l = l * alpha + rs;
         if (__any_sync(0xffffffffu, rescale)) {
           // O may be rescaled only once the previous P V has landed in it
-          if (j > 0 &&
+          if (jj > 0 &&
               !(ok = wait(&ctl->o_done[(g - 1) % pf::kSBufs], ((g - 1) / pf::kSBufs) & 1u)))
             break;
           tc_fence_after();
@@ -494,58 +539,117 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
         tc_fence_before();
         mbar_arrive(&ctl->p_full[b]);
       }
-      // epilogue: the thread's columns of O divided by the row sum (of both halves)
+      // Epilogue: the thread's columns of O divided by the row sum (of both halves), to the
+      // output, or (a split tile) to the item's partial with its log-sum-exp in the log2
+      // domain, which the merge kernel combines after the split-KV kernel.
       if (ok && live) {
         float lt;
         ok = exchange(l, true, &lt);
         l = lt;
       }
-      const uint32_t g_last = tc + I.nkv - 1;
-      if (ok && live && wait(&ctl->o_done[g_last % pf::kSBufs], (g_last / pf::kSBufs) & 1u)) {
+      // Each warp stages its 32 rows in the (now idle) K stages, swizzled by row so that
+      // neither the row-wise writes nor the chunk-wise reads conflict on banks, and then
+      // writes them back a whole row (or two, four) per instruction, coalesced.
+      const bool split = I.ns > 1;
+      const uint32_t g_last = tc + I.nj - 1;
+      const int sw = warp - 2 - (warp > pf::kVWarp ? 1 : 0);  // softmax warp index
+      uint8_t* stage = smem + pf::kK + sw * (32 * kC * 4);
+      const bool have =
+          ok && live && wait(&ctl->o_done[g_last % pf::kSBufs], (g_last / pf::kSBufs) & 1u);
+      if (have) {
         tc_fence_after();
         const float inv = (row_ok && l > 0.f) ? 1.f / l : 0.f;
-        const int64_t orow = static_cast<int64_t>(I.t0 + tok) * p.num_q_heads + I.h * G + r % G;
         uint32_t o[kC];
 #pragma unroll
         for (int c = 0; c < kC / 32; ++c)
           tmem_ld32(tl + pf::kOCol + hc + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&o[c * 32]));
         tmem_wait_ld();
-        if (row_ok) {
-          if (p.out_bf16) {
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
-                                                  orow * 128 + hc);
+        const bool bf16 = p.out_bf16 && !split;   // partials are fp32
+        if (split && half == 0 && row_ok)
+          p.part_lse[(static_cast<int64_t>(I.t0 + tok) * p.num_q_heads + I.h * G + r % G) *
+                         p.pmax + I.k] =
+              (seen && l > 0.f) ? m_used + __log2f(l) : -CUDART_INF_F;
+        if (!bf16) {
+          constexpr int CH = kC / 4;   // 16-byte chunks of the thread's row part
 #pragma unroll
-            for (int i = 0; i < kC / 8; ++i) {
-              uint32_t w[4];
+          for (int c = 0; c < CH; ++c)
+            *reinterpret_cast<uint4*>(stage + lane * CH * 16 + ((c ^ lane) & (CH - 1)) * 16) =
+                make_uint4(__float_as_uint(__uint_as_float(o[4 * c]) * inv),
+                           __float_as_uint(__uint_as_float(o[4 * c + 1]) * inv),
+                           __float_as_uint(__uint_as_float(o[4 * c + 2]) * inv),
+                           __float_as_uint(__uint_as_float(o[4 * c + 3]) * inv));
+        } else {
+          constexpr int CH = kC / 8;
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                w[e] = pack_bf16x2(__uint_as_float(o[8 * i + 2 * e]) * inv,
-                                   __uint_as_float(o[8 * i + 2 * e + 1]) * inv);
-              dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-          } else {
-            float4* dst =
-                reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + orow * 128 + hc);
-#pragma unroll
-            for (int i = 0; i < kC / 4; ++i)
-              dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv,
-                                   __uint_as_float(o[4 * i + 1]) * inv,
-                                   __uint_as_float(o[4 * i + 2]) * inv,
-                                   __uint_as_float(o[4 * i + 3]) * inv);
-          }
+          for (int c = 0; c < CH; ++c)
+            *reinterpret_cast<uint4*>(stage + lane * CH * 16 + ((c ^ lane) & (CH - 1)) * 16) =
+                make_uint4(pack_bf16x2(__uint_as_float(o[8 * c]) * inv,
+                                       __uint_as_float(o[8 * c + 1]) * inv),
+                           pack_bf16x2(__uint_as_float(o[8 * c + 2]) * inv,
+                                       __uint_as_float(o[8 * c + 3]) * inv),
+                           pack_bf16x2(__uint_as_float(o[8 * c + 4]) * inv,
+                                       __uint_as_float(o[8 * c + 5]) * inv),
+                           pack_bf16x2(__uint_as_float(o[8 * c + 6]) * inv,
+                                       __uint_as_float(o[8 * c + 7]) * inv));
         }
+        __syncwarp();
+        // this lane's row: its destination (NULL past the run), handed to the other lanes by
+        // shuffles in the write loop
+        const int64_t orow = static_cast<int64_t>(I.t0 + tok) * p.num_q_heads + I.h * G + r % G;
+        uint8_t* my_dst =
+            !row_ok ? nullptr
+            : split ? reinterpret_cast<uint8_t*>(p.part_o + (orow * p.pmax + I.k) * 128 + hc)
+            : bf16  ? reinterpret_cast<uint8_t*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                                 orow * 128 + hc)
+                    : reinterpret_cast<uint8_t*>(reinterpret_cast<float*>(p.out) + orow * 128 + hc);
+        const uint32_t stage_s = smem_u32(stage);
+        auto write_rows = [&](auto ch_tag) {
+          constexpr int CH = decltype(ch_tag)::value;
+          constexpr int RPI = 32 / CH;  // rows per instruction
+#pragma unroll 8
+          for (int it = 0; it < CH; ++it) {
+            const int rr = it * RPI + lane / CH, c = lane % CH;
+            uint4 v;
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                         : "r"(stage_s + rr * CH * 16 + ((c ^ rr) & (CH - 1)) * 16));
+            uint8_t* dst = reinterpret_cast<uint8_t*>(__shfl_sync(
+                0xffffffffu, reinterpret_cast<unsigned long long>(my_dst), rr));
+            if (dst) *reinterpret_cast<uint4*>(dst + c * 16) = v;
+          }
+        };
+        if (!bf16) write_rows(std::integral_constant<int, kC / 4>());
+        else write_rows(std::integral_constant<int, kC / 8>());
       }
+      fence_proxy_async_smem();  // generic accesses to the K stages before the next copies
       tc_fence_before();
     }
-    tc += I.nkv;
+    tc += I.nj;
     ++ic;
     __syncthreads();
     tc_fence_after();
+  }
+  // Exit, normal or after an expired wait: no copy may still be landing in shared memory and
+  // no MMA may still be using tensor memory when the CTA ends.
+  if (warp == 0 || warp == pf::kVWarp) {
+    // the latest fill of each stage is the only one that can still be in flight
+    const uint32_t iss = warp == 0 ? kiss : viss;
+    uint64_t* full = warp == 0 ? ctl->k_full : ctl->v_full;
+    for (uint32_t g = iss > pf::kStages ? iss - pf::kStages : 0; g < iss; ++g)
+      mbar_wait(&full[g % pf::kStages], (g / pf::kStages) & 1u, p.wait_ns);
+    if (warp == 0 && qiss) mbar_wait(&ctl->q_full, (qiss - 1) & 1u, p.wait_ns);
+  } else if (warp == 1) {
+    if (lane == 0) tc_commit(&ctl->drain);
+    __syncwarp();
+    mbar_wait(&ctl->drain, 0, p.wait_ns);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, pf::kTmemCols);
+  if (p.span && threadIdx.x == 0)
+    atomicMax(reinterpret_cast<unsigned long long*>(p.span) + 1,
+              static_cast<unsigned long long>(global_ns()));
 }
 
 namespace {
@@ -557,22 +661,23 @@ cudaError_t launch_prefill_as(const AttnArgs& a, const PrefillParams& p, const C
   LaunchInfo li;
   cudaError_t e = launch_info(prefill_kernel<kSplit>, kThreads, kSmem, &li);
   if (e != cudaSuccess) return e;
+  // at most one CTA per SM (shared memory); the plan decides how many of them work
   const int64_t upper =
-      static_cast<int64_t>(a.num_kv_heads) *
+      static_cast<int64_t>(a.num_kv_heads) * kMaxSplits *
       ((static_cast<int64_t>(a.num_q_tokens) * p.group + pf::kRows - 1) / pf::kRows +
        a.num_seqs);
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(upper, li.sms));
   if (a.pf_before && a.pf_after) cudaEventRecord(a.pf_before, a.stream);
-  prefill_kernel<kSplit>
-      <<<static_cast<unsigned>(grid), kThreads, kSmem, a.stream>>>(qmap, kmap, vmap, p);
+  e = launch_dependent(prefill_kernel<kSplit>, dim3(static_cast<unsigned>(grid)),
+                       dim3(kThreads), kSmem, a.stream, qmap, kmap, vmap, p);
   if (a.pf_before && a.pf_after) cudaEventRecord(a.pf_after, a.stream);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const AttnArgs& a, const int32_t* item_start, WsHeader* hdr,
-                           const PoolMaps& maps) {
+                           const PoolMaps& maps, const PrefillScratch& scratch) {
   PrefillParams p{};
   p.block_tables = a.block_tables;
   p.context_lens = a.context_lens;
@@ -590,12 +695,16 @@ cudaError_t launch_prefill(const AttnArgs& a, const int32_t* item_start, WsHeade
   p.score_log2 = a.scale * 1.4426950408889634f;
   p.wait_ns = a.wait_ns;
   p.skip_copy = a.skip_copy;
+  p.span = a.span ? a.span + 2 : nullptr;
+  p.part_lse = scratch.part_lse;
+  p.part_o = scratch.part_o;
+  p.pmax = scratch.pmax;
   // Runs of at most 64 rows (tokens x group heads: speculative verify) leave at least two of
   // a tile's four lane quarters empty; splitting each row over two warps then puts a second
   // warp on the busy quarters' SM sub-partitions.  Fuller tiles gain nothing from the split.
-  if (!prefill_uses_pairs(a.max_query_len, p.group))
-    return launch_prefill_as<true>(a, p, maps.q3, maps.k2, maps.v2);
-  return launch_chunk(a, p, maps.q3, maps.k4, maps.v4);
+  if (prefill_rows_split(a.max_query_len, p.group))
+    return launch_prefill_as<true>(a, p, maps.q3, maps.k4, maps.v4);
+  return launch_prefill_as<false>(a, p, maps.q3, maps.k4, maps.v4);
 }
 
 }  // namespace pa

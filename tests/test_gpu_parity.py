@@ -126,6 +126,30 @@ def test_prefill_chunks_on_tensor_core_tiles(hq, hkv):
     _check_small(w)
 
 
+@pytest.mark.parametrize("hq,hkv,out", [(32, 8, "f32"), (8, 8, "f32"), (64, 8, "f32"),
+                                         (32, 8, "bf16")])
+def test_prefill_tiles_split_along_the_keys(hq, hkv, out):
+    """Tiles whose keys span many 128-key slices are cut along the keys into up to four items;
+    each writes a normalised partial and its log-sum-exp, and the last to finish merges them.
+    Runs here: a 200-token chunk after a 4,800-token prefix (four splits), a 96-token chunk
+    after 1,200 (two), a short chunk with no prefix (none), beside decodes; sharp scores
+    (scale 1) make the partials' maxima differ widely."""
+    w = make_workload([5000, 1296, 700, 3000, 40], [200, 96, 130, 1, 1], num_q_heads=hq,
+                      num_kv_heads=hkv, head_dim=128, seed=hq + 13, pool_fill="nan")
+    _check_small(w, torch.bfloat16 if out == "bf16" else torch.float32)
+    w = make_workload([5000, 1296], [200, 96], num_q_heads=hq, num_kv_heads=hkv, head_dim=128,
+                      seed=hq + 14, pool_fill="nan", scale=1.0)
+    _check_small(w)
+
+
+def test_verify_tiles_split_along_the_keys():
+    """Speculative-verify runs (rows split over two softmax warps) over long contexts are cut
+    along the keys as well; every row of every split tile is merged and compared."""
+    w = make_workload([4096, 3000, 1100, 512], [5, 5, 5, 5], num_q_heads=32, num_kv_heads=8,
+                      head_dim=128, seed=57, pool_fill="nan")
+    _check_small(w)
+
+
 @pytest.mark.parametrize("qlens,ctx,dtype", [
     ([1, 1, 1, 1], [4000, 2000, 513, 100], "bf16"),        # split-KV decode
     ([1, 1, 1, 1], [4000, 2000, 513, 100], "fp8_e4m3"),
