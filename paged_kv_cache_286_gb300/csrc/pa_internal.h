@@ -171,12 +171,6 @@ struct PoolMaps {
   bool has_k4 = false, has_q3 = false;
 };
 
-// Whether the step's prefill tiles take the kernel instance with each row split over two
-// softmax warps: when every run has at most 64 (token x head) rows, as in speculative verify.
-inline bool prefill_rows_split(int32_t max_query_len, int32_t group) {
-  return static_cast<int64_t>(max_query_len) * group <= 64;
-}
-
 cudaError_t launch_prefill(const AttnArgs& a, const int32_t* item_start, WsHeader* hdr,
                            const PoolMaps& maps, const PrefillScratch& scratch);
 

@@ -25,25 +25,27 @@
 //    tile is [2 row groups][2 halves][8 rows][128 bytes] with the 128-byte swizzle, i.e. 8-key
 //    groups 2 KiB apart and the column halves 1 KiB apart, which the MMA descriptors express
 //    as strides.
-//  * Warp 1 issues tcgen05.mma from one thread: S = Q K^T into one of three TMEM buffers
-//    (128 x 128 fp32), and O += P V into a fourth, with P read from TMEM and V from shared
-//    memory (MN-major).  S of the next two slices is computed while the softmax works on the
-//    current one.  The softmax threads write P back over their S columns as bf16 hi and lo
-//    parts (keys 0-63: hi in columns 0-31, lo in 32-63; keys 64-127 likewise in 64-127), so
-//    P V is exact to ~2^-16 like the decode path.
-//  * Softmax, one thread per row (TMEM lane): it reads its row of S from TMEM once, masks keys
+//  * tcgen05.mma, each issued from one thread: warp 1 S = Q K^T into a TMEM buffer (128 x 128
+//    fp32), warp 7 O += P V into another, with P read from TMEM and V from shared memory
+//    (MN-major).  With one issuing thread for both, every wait of that thread sat between
+//    two groups of MMAs while the tensor pipe ran dry; with two, each waits on its own.  The softmax threads write P as bf16 hi and lo parts (keys 0-63: hi in
+//    columns 0-31, lo in 32-63; keys 64-127 likewise in 64-127; P V is exact to ~2^-16 like
+//    the decode path) into one of two P buffers.  They read each S into registers and hand
+//    the buffer back at once, so S of slice j+1 is computed while the softmax works on slice
+//    j, and the softmax never waits for the P V of the slice before to free a buffer.  TMEM:
+//    S 128 columns, P 2 x 128, O 128.
+//  * Softmax, two threads per row (TMEM lane), one for keys (and O columns) 0-63 in warps 2-5
+//    and one for 64-127 in warps 8-11: each reads its half row of S from TMEM once, masks keys
 //    beyond the row's position, keeps the running max in the log2 domain (set by the first
 //    slice that shows the row a key) and rescales O in TMEM only when the max grows by more
 //    than 2^8 (the final division uses the same max, so the result is exact), and finally
-//    divides O by the row sum.  Warps 2-5 do this for whole rows.  When every run has at most
-//    64 rows (speculative verify), at most two of the four lane quarters hold rows, and the
-//    kernel instance with the row split runs instead: warps 2-5 take keys (and O columns)
-//    0-63 and warps 7-10 keys 64-127, the two threads of a row agreeing on its max, and at the
-//    end adding their sums, through a shared-memory slot and an mbarrier of the pair.  A warp
-//    can only reach the lane quarter of its own SM sub-partition, so the split puts a second
-//    warp on each busy sub-partition to hide the latency of the exponentials and TMEM traffic.
+//    divides O by the row sum.  The two threads of a row agree on its max, and at the end add
+//    their sums, through a shared-memory slot and an mbarrier of the pair.  A warp can only
+//    reach the lane quarter of its own SM sub-partition; the per-slice work of a row is
+//    bound by instruction latency rather than issue, and the second warp on each
+//    sub-partition hides it (whole rows on one warp each took a quarter longer per slice).
 //  * V rows past the last valid key (stale slots, possibly NaN) are zeroed in shared memory
-//    before P V reads them; K there only feeds masked scores.
+//    before P V reads them (by the P V issuer's warp); K there only feeds masked scores.
 //  * The epilogue stages each warp's rows in the idle K stages (swizzled) and writes whole
 //    rows per instruction, instead of one scattered 16-byte piece per row and instruction.
 //  * Launched right after the plan (programmatic dependent launch): the CTAs beyond the SMs
@@ -65,7 +67,7 @@ namespace pf {
 constexpr int kRows = 128;
 constexpr int kKeys = 128;
 constexpr int kStages = 3;   // K and V ring depth
-constexpr int kSBufs = 3;    // S/P buffers in TMEM (3 x 128 columns) ahead of O
+constexpr int kPBufs = 2;    // P buffers in TMEM, after the S buffer
 constexpr int kHalf = 16384;  // one 64-column half of the q tile
 constexpr int kTile = 32768;  // 128 x 128 bf16
 constexpr int kBlockBytes = 4096;  // one (block, kv head) tile of a K or V stage
@@ -75,16 +77,15 @@ constexpr int kXBar = kCtl + 384;           // 4 mbarriers: one per pair of soft
 constexpr int kXSlot = kXBar + 32;          // 3 x 128 row slots of the pairs' exchanges
 constexpr int kXBufs = 3;
 constexpr int kVWarp = 6;     // V producer (warp 0 loads q and K)
-// Without the row split: warps 2-5 are the softmax, a thread a whole row.  With it: warps 2-5
-// take keys 0-63 of their rows and warps 7-10 keys 64-127, and the pairs exchange row sums
-// and maxima through shared memory.
-__host__ __device__ constexpr int threads(bool split) { return split ? 352 : 224; }
-__host__ __device__ constexpr int softmax_threads(bool split) { return split ? 256 : 128; }
-__host__ __device__ constexpr int smem_bytes(bool split) {
-  return 1024 + (split ? kXSlot + kXBufs * kRows * 4 : kCtl + 384);
-}
+constexpr int kPvWarp = 7;    // P V issuer (warp 1 issues S)
+// The softmax: warps 2-5 take keys 0-63 of their rows and warps 8-11 keys 64-127, and the
+// pairs exchange row sums and maxima through shared memory.
+constexpr int kThreads = 384;
+constexpr int kSoftmaxThreads = 256;
+constexpr int kSmemBytes = 1024 + kXSlot + kXBufs * kRows * 4;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kOCol = kSBufs * 128;
+constexpr uint32_t kSCol = 0, kPCol = 128, kOCol = kPCol + kPBufs * 128;
+static_assert(kOCol + 128 == kTmemCols, "TMEM columns");
 constexpr float kRescaleLog2 = 8.f;
 }  // namespace pf
 
@@ -96,7 +97,7 @@ struct PfItem {
 
 struct PfCtl {
   uint64_t q_full, k_full[pf::kStages], k_empty[pf::kStages], v_full[pf::kStages],
-      v_empty[pf::kStages], s_full[pf::kSBufs], p_full[pf::kSBufs], o_done[pf::kSBufs], drain;
+      v_empty[pf::kStages], s_full, s_free, p_full[pf::kPBufs], o_done[pf::kPBufs], drain[2];
   uint32_t tmem_base;
   int abort_flag;
   int v_zero_from[pf::kStages];
@@ -104,7 +105,7 @@ struct PfCtl {
   PfItem item[2];  // the current item and the next one, by the parity of the item count
 };
 static_assert(sizeof(PfCtl) <= 384, "control block too large");
-static_assert(pf::smem_bytes(true) <= 232448, "more shared memory than a CTA may have");
+static_assert(pf::kSmemBytes <= 232448, "more shared memory than a CTA may have");
 
 // Floats mapped to ints of the same order (an involution), so that integer atomicMax takes the
 // max of floats.  The empty slot INT_MIN is below every mapped float and reads as -0.0f.
@@ -114,6 +115,15 @@ __device__ __forceinline__ int float_order_key(float f) {
 }
 __device__ __forceinline__ float order_key_float(int k) {
   return __int_as_float(k >= 0 ? k : (k ^ 0x7fffffff));
+}
+
+// A thread's kC consecutive 32-bit TMEM columns from `cols` (its lane) into registers.
+template <int kC>
+__device__ __forceinline__ void tmem_ld_row(uint32_t cols, uint32_t (&v)[kC]) {
+#pragma unroll
+  for (int c = 0; c < kC / 32; ++c)
+    tmem_ld32(cols + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
+  tmem_wait_ld();
 }
 
 // Claims the next item from the counter (longest items, the last tiles of the last runs,
@@ -160,8 +170,7 @@ __device__ __forceinline__ PfItem claim_item(const PrefillParams& p, int total) 
   return it;
 }
 
-template <bool kSplit>
-__global__ void __launch_bounds__(pf::threads(kSplit), 1)
+__global__ void __launch_bounds__(pf::kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
@@ -188,16 +197,18 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
       mbar_init(&ctl->v_full[i], 1);
       mbar_init(&ctl->v_empty[i], 1);
     }
-    // one of each per S/P buffer, so that every waiter is within one phase of its barrier:
-    // S of tile g+3 is issued only after P V of tile g, which waits for P of tile g
-    for (int i = 0; i < pf::kSBufs; ++i) {
-      mbar_init(&ctl->s_full[i], 1);
-      mbar_init(&ctl->p_full[i], pf::softmax_threads(kSplit));
+    // S of slice g+1 is issued only once the softmax has read S of slice g (s_free), and the
+    // softmax writes P of slice g+2 only once P V of slice g has run: one p_full / o_done per
+    // P buffer keeps every waiter within one phase of its barrier
+    mbar_init(&ctl->s_full, 1);
+    mbar_init(&ctl->s_free, pf::kSoftmaxThreads);
+    for (int i = 0; i < pf::kPBufs; ++i) {
+      mbar_init(&ctl->p_full[i], pf::kSoftmaxThreads);
       mbar_init(&ctl->o_done[i], 1);
     }
-    mbar_init(&ctl->drain, 1);
-    if (kSplit)
-      for (int q = 0; q < 4; ++q)
+    mbar_init(&ctl->drain[0], 1);
+    mbar_init(&ctl->drain[1], 1);
+    for (int q = 0; q < 4; ++q)
         mbar_init(reinterpret_cast<uint64_t*>(smem + pf::kXBar) + q, 2);  // one lane a warp
     ctl->abort_flag = 0;
     fence_barrier_init();
@@ -207,8 +218,7 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
     ctl->item[0] = claim_item(p, total);
   }
   int* xslot = reinterpret_cast<int*>(smem + pf::kXSlot);  // [kXBufs][kRows], split only
-  if (kSplit)
-    for (int i = tid; i < pf::kXBufs * pf::kRows; i += pf::threads(true)) xslot[i] = INT_MIN;
+  for (int i = tid; i < pf::kXBufs * pf::kRows; i += pf::kThreads) xslot[i] = INT_MIN;
   if (warp == 1) tmem_alloc(&ctl->tmem_base, pf::kTmemCols);
   tc_fence_before();
   __syncthreads();
@@ -316,13 +326,15 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
         }
       }
     } else if (warp == 1) {
-      // ------------------------------------------------------------- MMA issuer ---------
+      // ------------------------------------------------------------- S issuer -----------
+      // S of slice jj into the S buffer once the softmax has read S of jj - 1 out of it.
       const uint32_t id_s = idesc_bf16_f32(128, 128, false);
-      const uint32_t id_pv = idesc_bf16_f32(128, 128, true);
       const uint32_t q_addr = smem_u32(smem + pf::kQ);
-      auto issue_s = [&](int jj) -> bool {
-        const uint32_t g = tc + jj, st = g % pf::kStages, b = g % pf::kSBufs;
-        if (!wait(&ctl->k_full[st], (g / pf::kStages) & 1u)) return false;
+      bool ok = wait(&ctl->q_full, ic & 1u);
+      for (int jj = 0; ok && jj < I.nj; ++jj) {
+        const uint32_t g = tc + jj, st = g % pf::kStages;
+        if (g > 0 && !(ok = wait(&ctl->s_free, (g - 1) & 1u))) break;
+        if (!(ok = wait(&ctl->k_full[st], (g / pf::kStages) & 1u))) break;
         tc_fence_after();
         if (lane == 0) {
           const uint32_t k_addr = smem_u32(smem + pf::kK + st * pf::kTile);
@@ -330,21 +342,23 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t qa = q_addr + (ks >> 2) * pf::kHalf + (ks & 3) * 32;
             const uint32_t kb = k_addr + (ks >> 2) * 1024 + (ks & 3) * 32;
-            tc_mma_bf16(tmem + b * 128u, smem_desc_sw128(qa, 16, 1024),
+            tc_mma_bf16(tmem + pf::kSCol, smem_desc_sw128(qa, 16, 1024),
                         smem_desc_sw128(kb, 16, 2048), id_s, ks > 0);
           }
-          tc_commit(&ctl->s_full[b]);
+          tc_commit(&ctl->s_full);
           tc_commit(&ctl->k_empty[st]);
         }
         __syncwarp();
-        return true;
-      };
-      bool ok = wait(&ctl->q_full, ic & 1u);
-      if (ok) tc_fence_after();
-      for (int jj = 0; ok && jj < min(pf::kSBufs, I.nj); ++jj) ok = issue_s(jj);
-      for (int jj = 0; ok && jj < I.nj; ++jj) {
-        const uint32_t g = tc + jj, st = g % pf::kStages, b = g % pf::kSBufs;
-        if (!(ok = wait(&ctl->v_full[st], (g / pf::kStages) & 1u))) break;
+      }
+    } else if (warp == pf::kPvWarp) {
+      // ------------------------------------------------------------- P V issuer ---------
+      // O += P V of slice jj once its V has landed (rows without a valid key cleared) and the
+      // softmax has handed over its P.  A warp of its own, so that neither issuer's waits hold
+      // back the other's MMAs.
+      const uint32_t id_pv = idesc_bf16_f32(128, 128, true);
+      for (int jj = 0; jj < I.nj; ++jj) {
+        const uint32_t g = tc + jj, st = g % pf::kStages, b = g % pf::kPBufs;
+        if (!wait(&ctl->v_full[st], (g / pf::kStages) & 1u)) break;
         uint8_t* vt = smem + pf::kV + st * pf::kTile;
         const int zf = ctl->v_zero_from[st];
         const uint32_t badm = ctl->v_bad[st];
@@ -360,7 +374,7 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
           fence_proxy_async_smem();
           __syncwarp();
         }
-        if (!(ok = wait(&ctl->p_full[b], (g / pf::kSBufs) & 1u))) break;
+        if (!wait(&ctl->p_full[b], (g / pf::kPBufs) & 1u)) break;
         tc_fence_after();
         if (lane == 0) {
           const uint32_t v_addr = smem_u32(vt);
@@ -368,7 +382,9 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
           // buffer and their lo parts in 32-63; keys 64-127 the same in columns 64-127.  V of
           // those keys: block ks of the stage, MN-major (the column halves 1 KiB apart, 8-key
           // groups 2 KiB apart).
-          auto p_col = [&](int ks) { return tmem + b * 128u + (ks >> 2) * 64u + (ks & 3) * 8u; };
+          auto p_col = [&](int ks) {
+            return tmem + pf::kPCol + b * 128u + (ks >> 2) * 64u + (ks & 3) * 8u;
+          };
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
             tc_mma_bf16_ts(tmem + pf::kOCol, p_col(ks),
@@ -382,14 +398,11 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
           tc_commit(&ctl->v_empty[st]);
         }
         __syncwarp();
-        // S of slice jj+3 reuses this slice's S/P buffer: it is issued after (and runs after)
-        // the P V that reads P from it
-        if (jj + pf::kSBufs < I.nj) ok = issue_s(jj + pf::kSBufs);
       }
     } else {
       // ------------------------------------------------------------- softmax rows -------
-      constexpr int kC = kSplit ? 64 : 128;  // keys (and O columns) of a thread
-      const int half = (kSplit && warp > pf::kVWarp) ? 1 : 0;
+      constexpr int kC = 64;  // keys (and O columns) of a thread
+      const int half = warp > pf::kPvWarp ? 1 : 0;
       const int quarter = warp & 3;        // TMEM lane quarter this warp may access
       const int r = quarter * 32 + lane;   // tile row = TMEM lane
       const int tok = r / G;
@@ -403,10 +416,6 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
       // warp's updates are ordered before it) and read the slot; then the slot that the
       // exchange after next uses is cleared (its last readers have passed this barrier).
       auto exchange = [&](float v, bool sum, float* out) -> bool {
-        if (!kSplit) {
-          *out = v;
-          return true;
-        }
         int* slot = xslot + (xc % pf::kXBufs) * pf::kRows + r;
         if (sum) atomicAdd(reinterpret_cast<float*>(slot), v);  // -0.0f + a + b, either order
         else atomicMax(slot, float_order_key(v));
@@ -424,30 +433,26 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
       const bool live = __any_sync(0xffffffffu, row_ok);
       float m_used = 0.f, l = 0.f;
       bool seen = false;  // whether m_used comes from a visible key yet
+      // This thread's columns of S.  S of a slice is read into registers and the buffer
+      // handed back (s_free) before the slice's P is worked out; a quarter with no row of the
+      // run reads nothing and leaves its rows of P alone (their O rows are never read).
+      const uint32_t s_cols = tl + pf::kSCol + hc;
       bool ok = true;
       for (int jj = 0; jj < I.nj; ++jj) {
-        const uint32_t g = tc + jj, b = g % pf::kSBufs;
-        if (!(ok = wait(&ctl->s_full[b], (g / pf::kSBufs) & 1u))) break;
+        const uint32_t g = tc + jj, b = g % pf::kPBufs;
+        if (!(ok = wait(&ctl->s_full, g & 1u))) break;
         tc_fence_after();
-        const uint32_t sb = tl + b * 128u + hc;  // this thread's columns of S, then of P
         if (!live) {
-          uint32_t z[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) z[e] = 0u;
-#pragma unroll
-          for (int c = 0; c < kC / 16; ++c) tmem_st16(sb + c * 16, z);
-          tmem_wait_st();
-          tc_fence_before();
+          mbar_arrive(&ctl->s_free);
           mbar_arrive(&ctl->p_full[b]);
           continue;
         }
+        uint32_t sv[kC];
+        tmem_ld_row<kC>(s_cols, sv);
+        tc_fence_before();
+        mbar_arrive(&ctl->s_free);
         // keys 0..kmax of this thread's columns are visible
         const int kmax = row_ok ? row_pos - (I.j0 + jj) * pf::kKeys - half * 64 : -1;
-        uint32_t sv[kC];
-#pragma unroll
-        for (int c = 0; c < kC / 32; ++c)
-          tmem_ld32(sb + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
-        tmem_wait_ld();
         // raw scores, masked keys -inf; the row max is taken on them (the scale is positive)
         // and moved to the log2 domain once.  Eight independent max / sum accumulators keep
         // the dependency chains short.
@@ -487,10 +492,17 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
           rescale = true;
         }
         const float alpha = rescale ? fast_exp2(m_used - m_new) : 1.f;
+        // The P buffer is free once the P V of two slices back has run (long since, as a
+        // rule: it was handed over a slice ago).
+        if (g >= pf::kPBufs &&
+            !(ok = wait(&ctl->o_done[b], ((g - pf::kPBufs) / pf::kPBufs) & 1u)))
+          break;
+        tc_fence_after();
         // probabilities 2^(s * scale * log2 e - m); for every 64 keys, bf16 hi parts into their
         // columns 0..31 and lo parts into 32..63.  The split is by truncation, on the integer
         // pipes: hi keeps the upper 16 bits of p, lo = p - hi exactly in fp32, and lo is
         // truncated in turn, so hi + lo = p within 2^-14 relative.
+        const uint32_t p_cols = tl + pf::kPCol + b * 128u + hc;
         float rsum[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) rsum[i] = 0.f;
@@ -508,7 +520,7 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
             const float l1 = p1 - __uint_as_float(b1 & 0xffff0000u);
             lo[e] = prmt(__float_as_uint(l0), __float_as_uint(l1), 0x7632u);
           }
-          const uint32_t pc = sb + (c >> 1) * 64 + (c & 1) * 16;
+          const uint32_t pc = p_cols + (c >> 1) * 64 + (c & 1) * 16;
           tmem_st16(pc, hi);
           tmem_st16(pc + 32, lo);
         }
@@ -516,9 +528,9 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
                          ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
         l = l * alpha + rs;
         if (__any_sync(0xffffffffu, rescale)) {
-          // O may be rescaled only once the previous P V has landed in it
-          if (jj > 0 &&
-              !(ok = wait(&ctl->o_done[(g - 1) % pf::kSBufs], ((g - 1) / pf::kSBufs) & 1u)))
+          // O may be rescaled only once the previous P V has landed in it (a rescale needs a
+          // visible key in an earlier slice of the item, so jj > 0)
+          if (!(ok = wait(&ctl->o_done[(g - 1) % pf::kPBufs], ((g - 1) / pf::kPBufs) & 1u)))
             break;
           tc_fence_after();
           uint32_t o[kC];
@@ -552,10 +564,10 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
       // writes them back a whole row (or two, four) per instruction, coalesced.
       const bool split = I.ns > 1;
       const uint32_t g_last = tc + I.nj - 1;
-      const int sw = warp - 2 - (warp > pf::kVWarp ? 1 : 0);  // softmax warp index
+      const int sw = half ? warp - 4 : warp - 2;  // softmax warp index 0..7
       uint8_t* stage = smem + pf::kK + sw * (32 * kC * 4);
       const bool have =
-          ok && live && wait(&ctl->o_done[g_last % pf::kSBufs], (g_last / pf::kSBufs) & 1u);
+          ok && live && wait(&ctl->o_done[g_last % pf::kPBufs], (g_last / pf::kPBufs) & 1u);
       if (have) {
         tc_fence_after();
         const float inv = (row_ok && l > 0.f) ? 1.f / l : 0.f;
@@ -638,10 +650,12 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
     for (uint32_t g = iss > pf::kStages ? iss - pf::kStages : 0; g < iss; ++g)
       mbar_wait(&full[g % pf::kStages], (g / pf::kStages) & 1u, p.wait_ns);
     if (warp == 0 && qiss) mbar_wait(&ctl->q_full, (qiss - 1) & 1u, p.wait_ns);
-  } else if (warp == 1) {
-    if (lane == 0) tc_commit(&ctl->drain);
+  } else if (warp == 1 || warp == pf::kPvWarp) {
+    // each issuer's own MMAs (a commit tracks those of the issuing thread)
+    uint64_t* drain = &ctl->drain[warp == 1 ? 0 : 1];
+    if (lane == 0) tc_commit(drain);
     __syncwarp();
-    mbar_wait(&ctl->drain, 0, p.wait_ns);
+    mbar_wait(drain, 0, p.wait_ns);
   }
   tc_fence_before();
   __syncthreads();
@@ -654,12 +668,10 @@ __global__ void __launch_bounds__(pf::threads(kSplit), 1)
 
 namespace {
 
-template <bool kSplit>
-cudaError_t launch_prefill_as(const AttnArgs& a, const PrefillParams& p, const CUtensorMap& qmap,
-                              const CUtensorMap& kmap, const CUtensorMap& vmap) {
-  constexpr int kThreads = pf::threads(kSplit), kSmem = pf::smem_bytes(kSplit);
+cudaError_t launch_prefill_grid(const AttnArgs& a, const PrefillParams& p, const CUtensorMap& qmap,
+                                const CUtensorMap& kmap, const CUtensorMap& vmap) {
   LaunchInfo li;
-  cudaError_t e = launch_info(prefill_kernel<kSplit>, kThreads, kSmem, &li);
+  cudaError_t e = launch_info(prefill_kernel, pf::kThreads, pf::kSmemBytes, &li);
   if (e != cudaSuccess) return e;
   // at most one CTA per SM (shared memory); the plan decides how many of them work
   const int64_t upper =
@@ -668,8 +680,8 @@ cudaError_t launch_prefill_as(const AttnArgs& a, const PrefillParams& p, const C
        a.num_seqs);
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(upper, li.sms));
   if (a.pf_before && a.pf_after) cudaEventRecord(a.pf_before, a.stream);
-  e = launch_dependent(prefill_kernel<kSplit>, dim3(static_cast<unsigned>(grid)),
-                       dim3(kThreads), kSmem, a.stream, qmap, kmap, vmap, p);
+  e = launch_dependent(prefill_kernel, dim3(static_cast<unsigned>(grid)), dim3(pf::kThreads),
+                       pf::kSmemBytes, a.stream, qmap, kmap, vmap, p);
   if (a.pf_before && a.pf_after) cudaEventRecord(a.pf_after, a.stream);
   return e;
 }
@@ -699,12 +711,7 @@ cudaError_t launch_prefill(const AttnArgs& a, const int32_t* item_start, WsHeade
   p.part_lse = scratch.part_lse;
   p.part_o = scratch.part_o;
   p.pmax = scratch.pmax;
-  // Runs of at most 64 rows (tokens x group heads: speculative verify) leave at least two of
-  // a tile's four lane quarters empty; splitting each row over two warps then puts a second
-  // warp on the busy quarters' SM sub-partitions.  Fuller tiles gain nothing from the split.
-  if (prefill_rows_split(a.max_query_len, p.group))
-    return launch_prefill_as<true>(a, p, maps.q3, maps.k4, maps.v4);
-  return launch_prefill_as<false>(a, p, maps.q3, maps.k4, maps.v4);
+  return launch_prefill_grid(a, p, maps.q3, maps.k4, maps.v4);
 }
 
 }  // namespace pa

@@ -170,6 +170,33 @@ def test_prefill_chunks_bf16_output():
     _check_small(w, out_dtype=torch.bfloat16)
 
 
+def test_large_v_values_keep_their_precision():
+    """V values far outside the N(0,1) range (+-65536, beyond what fp16 can hold, and 65280)
+    in tensor-core tiles: P V stays exact (bf16 hi + lo parts of P against bf16 V), so the
+    output is finite and the dims holding them are within 2^-13 of their size, the rest
+    within 2e-3."""
+    w = make_workload([600, 300], [200, 100], num_q_heads=32, num_kv_heads=8, head_dim=128,
+                      seed=77)
+    # prior rows: sequence 0 positions 0..399, then sequence 1 positions 0..199
+    planted = {(10, 0, 5): 0x4780,    # +65536: keys 0-63 of slice 0 of sequence 0, head 0
+               (300, 3, 7): 0xC780,   # -65536: keys 0-63 of slice 2, head 3
+               (405, 2, 9): 0x477F}   # 65280: sequence 1, head 2
+    for (i, hk, d), bits in planted.items():
+        w.v_prior_bits[i, hk, d] = bits
+    dev, out = _h().run_gpu(w, torch.float32)
+    _, _, ref = run_step(w)
+    got = out.float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(got).all(), "non-finite output"
+    G = w.num_q_heads // w.num_kv_heads
+    mask = np.zeros(ref.shape, dtype=bool)
+    err = np.abs(got - ref)
+    for (_, hk, d), bits in planted.items():
+        mask[:, hk * G:(hk + 1) * G, d] = True
+        e, r = err[:, hk * G:(hk + 1) * G, d], np.abs(ref[:, hk * G:(hk + 1) * G, d])
+        assert np.all(e <= 2e-3 + 2.0 ** -13 * r), (hex(bits), float((e - 2.0 ** -13 * r).max()))
+    assert err[~mask].max() <= 2e-3, err[~mask].max()
+
+
 def test_prefill_block_permutation_is_bitwise_invariant():
     h = _h()
     args = dict(num_q_heads=32, num_kv_heads=8, head_dim=128, seed=92, pool_factor=1.5)
