@@ -179,6 +179,8 @@ WsLayout workspace_layout(int32_t S, int32_t T, int32_t Hq, int32_t Hkv, int32_t
   off = up(off + sizeof(int32_t) * (size_t(std::max(S, 0)) + 1));
   w.pf_item_start = off;
   off = up(off + sizeof(int32_t) * (size_t(std::max(S, 0)) + 1));
+  w.pf_order = off;
+  off = up(off + sizeof(int32_t) * size_t(std::max(S, 1)));
   w.merge_start = off;
   off = up(off + sizeof(int32_t) * (size_t(std::max(S, 0)) + 1));
   const size_t rows = size_t(std::max(T, 0)) * size_t(std::max(Hq, 0));

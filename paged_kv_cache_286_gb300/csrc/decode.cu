@@ -46,7 +46,8 @@ struct DecodeParams {
   const int32_t* context_lens;
   const int32_t* qsl;
   int32_t* item_start;
-  int32_t* pf_item_start;
+  int32_t* pf_item_start;  // [S+1] prefill item prefix sums over the runs in claim order
+  int32_t* pf_order;       // [S] the runs with prefill items, longest item first
   int32_t* merge_start;    // [S+1] prefix sums of the rows the merge combines
   float* part_lse;
   float* part_o;
@@ -123,8 +124,10 @@ __device__ __forceinline__ int prefill_items_of(const DecodeParams& p, int n, in
 __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
   grid_launch_dependents();  // the attention kernel may set up its CTAs meanwhile
   grid_dependency_wait();    // every earlier kernel of the stream is complete and visible
-  constexpr int kN = 3;      // decode items, prefill items, merge rows
+  constexpr int kN = 4;      // decode items, prefill items, merge rows, runs with prefill items
+  constexpr int kSortMax = 2048;  // runs the plan orders by length (more: sequence order)
   __shared__ int warp_sums[32][kN];
+  __shared__ int sort_key[kSortMax], sort_val[kSortMax];
   __shared__ int carry_s[kN];
   __shared__ float red_f[32][3];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -149,6 +152,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
                 (cnt[1] > 0 && prefill_splits(n, L, p.group, p.pmax) > 1))
                    ? n * p.num_q_heads
                    : 0;
+      cnt[3] = cnt[1] > 0 ? 1 : 0;
       if (cnt[0] > 0) dec_bytes += float(ceil_div(L, kBlockSize)) * p.num_kv_heads *
                                    float(p.kv_tile_bytes);
       if (cnt[1] > 0) {
@@ -198,14 +202,87 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
       excl[k] = carry_s[k] + (warp ? warp_sums[warp - 1][k] : 0) + x[k] - cnt[k];
     if (s < p.num_seqs) {
       p.item_start[s] = excl[0];
-      p.pf_item_start[s] = excl[1];
       p.merge_start[s] = excl[2];
+      if (cnt[3]) p.pf_order[excl[3]] = s;  // runs with prefill items, in sequence order
     }
     __syncthreads();
     if (tid == 1023)
 #pragma unroll
       for (int k = 0; k < kN; ++k) carry_s[k] = excl[k] + cnt[k];
     __syncthreads();
+  }
+  // Claim order of the prefill runs: longest item first (its 128-key slices; ties by sequence),
+  // so that the CTAs taking items from the counter end close together.  A bitonic sort in
+  // shared memory, padded to a power of two with entries that sort last.
+  const int R = carry_s[3];
+  auto longest_item = [&](int s) {
+    const int n = p.qsl[s + 1] - p.qsl[s];
+    const int L = p.context_lens[s];
+    return ceil_div((L - 1) / 128 + 1, prefill_splits(n, L, p.group, p.pmax));
+  };
+  if (R > 1 && R <= kSortMax) {
+    int n2 = 2;
+    while (n2 < R) n2 <<= 1;
+    for (int i = tid; i < n2; i += 1024) {
+      sort_key[i] = i < R ? longest_item(p.pf_order[i]) : -1;
+      sort_val[i] = i < R ? p.pf_order[i] : INT_MAX;
+    }
+    __syncthreads();
+    for (int k = 2; k <= n2; k <<= 1)
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        for (int i = tid; i < n2; i += 1024) {
+          const int ixj = i ^ j;
+          if (ixj > i) {
+            const int ka = sort_key[i], kb = sort_key[ixj], va = sort_val[i], vb = sort_val[ixj];
+            const bool a_first = ka > kb || (ka == kb && va < vb);
+            const bool b_first = kb > ka || (kb == ka && vb < va);
+            if ((i & k) == 0 ? b_first : a_first) {
+              sort_key[i] = kb;
+              sort_key[ixj] = ka;
+              sort_val[i] = vb;
+              sort_val[ixj] = va;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    for (int i = tid; i < R; i += 1024) p.pf_order[i] = sort_val[i];
+  }
+  __syncthreads();
+  // prefix sums of the prefill items over the runs in that order; ranks R .. S hold the total
+  {
+    int carry = 0;
+    for (int base = 0; base < R; base += 1024) {
+      const int r = base + tid;
+      int c = 0;
+      if (r < R) {
+        const int s = p.pf_order[r];
+        c = prefill_items_of(p, p.qsl[s + 1] - p.qsl[s], p.context_lens[s]);
+      }
+      int x = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) warp_sums[warp][0] = x;
+      __syncthreads();
+      if (warp == 0) {
+        int w = warp_sums[lane][0];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, w, o);
+          if (lane >= o) w += y;
+        }
+        warp_sums[lane][0] = w;
+      }
+      __syncthreads();
+      const int excl = carry + (warp ? warp_sums[warp - 1][0] : 0) + x - c;
+      if (r < R) p.pf_item_start[r] = excl;
+      carry += warp_sums[31][0];
+      __syncthreads();
+    }
+    for (int r = R + tid; r <= p.num_seqs; r += 1024) p.pf_item_start[r] = carry_s[1];
   }
   // block reduction of the cost model
 #pragma unroll
@@ -247,7 +324,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
       }
     }
     p.item_start[p.num_seqs] = carry_s[0];
-    p.pf_item_start[p.num_seqs] = carry_s[1];
     p.merge_start[p.num_seqs] = carry_s[2];
     p.hdr->decode_counter = 0;
     p.hdr->prefill_counter = 0;
@@ -967,6 +1043,7 @@ cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const PoolMa
   p.qsl = a.query_start_loc;
   p.item_start = reinterpret_cast<int32_t*>(wsb + ws.item_start);
   p.pf_item_start = reinterpret_cast<int32_t*>(wsb + ws.pf_item_start);
+  p.pf_order = reinterpret_cast<int32_t*>(wsb + ws.pf_order);
   p.merge_start = reinterpret_cast<int32_t*>(wsb + ws.merge_start);
   p.part_lse = reinterpret_cast<float*>(wsb + ws.part_lse);
   p.part_o = reinterpret_cast<float*>(wsb + ws.part_o);
@@ -1027,7 +1104,9 @@ cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const PoolMa
   // only read what the plan and the append wrote, and write disjoint output rows.
   if (prefill) {
     PrefillScratch scratch{p.part_lse, p.part_o, p.pmax};
-    if ((e = launch_prefill(a, p.pf_item_start, p.hdr, maps, scratch)) != cudaSuccess) return e;
+    if ((e = launch_prefill(a, p.pf_item_start, p.pf_order, p.hdr, maps, scratch)) !=
+        cudaSuccess)
+      return e;
     p.wait_at_end = 1;
   }
   if (fp8 && hpi == 2)

@@ -61,7 +61,8 @@ struct AttnArgs {
 // Workspace carve-up; a pure function of the step's shape (see workspace_layout).
 struct WsLayout {
   size_t item_start;  // int32 [num_seqs + 1], decode work-item prefix sums
-  size_t pf_item_start;  // int32 [num_seqs + 1], prefill work-item prefix sums
+  size_t pf_item_start;  // int32 [num_seqs + 1], prefill work-item prefix sums, by claim rank
+  size_t pf_order;    // int32 [num_seqs], the sequence of each prefill claim rank
   size_t merge_start;  // int32 [num_seqs + 1], prefix sums of the rows (token x q head) that
                        // the merge combines: those of split-KV sequences with 2+ partitions
   size_t part_lse;    // float [num_q_tokens][num_q_heads][pmax], log2-domain log-sum-exp
@@ -137,7 +138,8 @@ struct PrefillParams {
   const int32_t* block_tables;
   const int32_t* context_lens;
   const int32_t* qsl;
-  const int32_t* item_start;  // [S+1] prefix sums of prefill items
+  const int32_t* item_start;  // [S+1] prefix sums of prefill items over the runs in claim order
+  const int32_t* order;       // [S] the sequence of each run in claim order
   void* out;
   WsHeader* hdr;
   int32_t max_blocks_per_seq;
@@ -171,7 +173,8 @@ struct PoolMaps {
   bool has_k4 = false, has_q3 = false;
 };
 
-cudaError_t launch_prefill(const AttnArgs& a, const int32_t* item_start, WsHeader* hdr,
+cudaError_t launch_prefill(const AttnArgs& a, const int32_t* item_start, const int32_t* order,
+                           WsHeader* hdr,
                            const PoolMaps& maps, const PrefillScratch& scratch);
 
 

@@ -126,32 +126,32 @@ __device__ __forceinline__ void tmem_ld_row(uint32_t cols, uint32_t (&v)[kC]) {
   tmem_wait_ld();
 }
 
-// Claims the next item from the counter (longest items, the last tiles of the last runs,
-// first) and decodes it.
+// Claims the next item from the counter and decodes it.  The plan ordered the runs longest
+// item first; within a run the items go from its last (longest) tile back.
 __device__ __forceinline__ PfItem claim_item(const PrefillParams& p, int total) {
   PfItem it;
-  const int rev = static_cast<int>(atomicAdd(&p.hdr->prefill_counter, 1u));
-  const int item = total - 1 - rev;
-  it.valid = item >= 0;
-  it.first = rev == 0;
+  const int item = static_cast<int>(atomicAdd(&p.hdr->prefill_counter, 1u));
+  it.valid = item < total;
+  it.first = item == 0;
   if (!it.valid) return it;
-  int lo = 0, hi = p.num_seqs;
+  int lo = 0, hi = p.num_seqs;  // the last rank whose first item is at or before this one
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (p.item_start[mid] <= item) lo = mid; else hi = mid;
   }
-  const int s = lo;
+  const int s = p.order[lo];
   const int t0 = p.qsl[s];
   const int n = p.qsl[s + 1] - t0;
   const int L = p.context_lens[s];
   const int tpt = pf::kRows / p.group;
-  const int qtiles = (n + tpt - 1) / tpt;
   const int ns = prefill_splits(n, L, p.group, p.pmax);
-  const int local = item - p.item_start[s];
+  // counted from the run's last item: the q tile is the outer index, so the last (longest)
+  // tiles of every kv head come first
+  const int local = p.item_start[lo + 1] - 1 - item;
   const int k = local % ns;
   const int ti = local / ns;
-  const int h = ti / qtiles;
-  const int qt = ti - h * qtiles;
+  const int h = ti % p.num_kv_heads;
+  const int qt = ti / p.num_kv_heads;
   const int i0 = qt * tpt;
   it.s = s;
   it.h = h;
@@ -688,13 +688,15 @@ cudaError_t launch_prefill_grid(const AttnArgs& a, const PrefillParams& p, const
 
 }  // namespace
 
-cudaError_t launch_prefill(const AttnArgs& a, const int32_t* item_start, WsHeader* hdr,
+cudaError_t launch_prefill(const AttnArgs& a, const int32_t* item_start, const int32_t* order,
+                           WsHeader* hdr,
                            const PoolMaps& maps, const PrefillScratch& scratch) {
   PrefillParams p{};
   p.block_tables = a.block_tables;
   p.context_lens = a.context_lens;
   p.qsl = a.query_start_loc;
   p.item_start = item_start;
+  p.order = order;
   p.out = a.out;
   p.hdr = hdr;
   p.max_blocks_per_seq = a.max_blocks_per_seq;
