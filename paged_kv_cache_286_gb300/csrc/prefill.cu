@@ -46,8 +46,14 @@
 //    sub-partition hides it (whole rows on one warp each took a quarter longer per slice).
 //  * V rows past the last valid key (stale slots, possibly NaN) are zeroed in shared memory
 //    before P V reads them (by the P V issuer's warp); K there only feeds masked scores.
-//  * The epilogue stages each warp's rows in the idle K stages (swizzled) and writes whole
+//  * The epilogue stages each warp's rows in a region of its own (swizzled) and writes whole
 //    rows per instruction, instead of one scattered 16-byte piece per row and instruction.
+//  * Items follow one another without a block-wide barrier: warp 0 claims the next item while
+//    the current one runs and loads its q tile and first K/V slices as soon as the S MMAs and
+//    stages of the current one are done with theirs, so the next item's first S is computed
+//    while the softmax warps write the current one's output; only its first P V waits for
+//    them to have read O.  (K and V rings of two stages make room for the staging region; the
+//    slice period did not change with the ring depth.)
 //  * Launched right after the plan (programmatic dependent launch): the CTAs beyond the SMs
 //    the plan gives this kernel end at once, and the split-KV kernel launches onto the rest.
 //  * Every wait is bounded; on expiry the CTA records PA_DEVERR_TIMEOUT, stops, lets the copies
@@ -66,13 +72,15 @@ namespace pa {
 namespace pf {
 constexpr int kRows = 128;
 constexpr int kKeys = 128;
-constexpr int kStages = 3;   // K and V ring depth
+constexpr int kStages = 2;   // K and V ring depth
 constexpr int kPBufs = 2;    // P buffers in TMEM, after the S buffer
 constexpr int kHalf = 16384;  // one 64-column half of the q tile
 constexpr int kTile = 32768;  // 128 x 128 bf16
 constexpr int kBlockBytes = 4096;  // one (block, kv head) tile of a K or V stage
 constexpr int kQ = 0, kK = kTile, kV = kK + kStages * kTile;
-constexpr int kCtl = kV + kStages * kTile;  // control block (barriers, items, flags)
+constexpr int kStage = kV + kStages * kTile;  // the epilogue's staging of the softmax warps' rows
+constexpr int kStageBytes = 65536;
+constexpr int kCtl = kStage + kStageBytes;    // control block (barriers, items, flags)
 constexpr int kXBar = kCtl + 384;           // 4 mbarriers: one per pair of softmax warps
 constexpr int kXSlot = kXBar + 32;          // 3 x 128 row slots of the pairs' exchanges
 constexpr int kXBufs = 3;
@@ -97,12 +105,13 @@ struct PfItem {
 
 struct PfCtl {
   uint64_t q_full, k_full[pf::kStages], k_empty[pf::kStages], v_full[pf::kStages],
-      v_empty[pf::kStages], s_full, s_free, p_full[pf::kPBufs], o_done[pf::kPBufs], drain[2];
+      v_empty[pf::kStages], s_full, s_free, p_full[pf::kPBufs], o_done[pf::kPBufs], drain[2],
+      q_empty, o_free, item_full[2], item_empty[2];
   uint32_t tmem_base;
   int abort_flag;
   int v_zero_from[pf::kStages];
   uint32_t v_bad[pf::kStages];
-  PfItem item[2];  // the current item and the next one, by the parity of the item count
+  PfItem item[2];  // by the parity of the item count: warp 0 fills one while the other is read
 };
 static_assert(sizeof(PfCtl) <= 384, "control block too large");
 static_assert(pf::kSmemBytes <= 232448, "more shared memory than a CTA may have");
@@ -208,6 +217,17 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     }
     mbar_init(&ctl->drain[0], 1);
     mbar_init(&ctl->drain[1], 1);
+    // Items flow through the roles without a block-wide barrier between them: warp 0 claims
+    // the next item into the other slot once the other warps have read the item that was
+    // there (item_empty: one lane of each of the 11), loads its q tile once the S MMAs of the
+    // item before have read theirs (q_empty), and the P V issuer starts the next item's O once
+    // the softmax warps have read the last one (o_free: one lane of each of the 8).
+    mbar_init(&ctl->q_empty, 1);
+    mbar_init(&ctl->o_free, pf::kSoftmaxThreads / 32);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctl->item_full[i], 1);
+      mbar_init(&ctl->item_empty[i], pf::kThreads / 32 - 1);
+    }
     for (int q = 0; q < 4; ++q)
         mbar_init(reinterpret_cast<uint64_t*>(smem + pf::kXBar) + q, 2);  // one lane a warp
     ctl->abort_flag = 0;
@@ -216,6 +236,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
     ctl->item[0] = claim_item(p, total);
+    mbar_arrive(&ctl->item_full[0]);
   }
   int* xslot = reinterpret_cast<int*>(smem + pf::kXSlot);  // [kXBufs][kRows], split only
   for (int i = tid; i < pf::kXBufs * pf::kRows; i += pf::kThreads) xslot[i] = INT_MIN;
@@ -242,20 +263,27 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
   };
 
   while (true) {
+    // warp 0 wrote the item itself; the others wait for it and hand the slot back once read
+    if (warp != 0 && !wait(&ctl->item_full[ic & 1u], (ic >> 1) & 1u)) break;
     const PfItem I = ctl->item[ic & 1u];
-    if (!I.valid || ctl->abort_flag) break;
+    if (warp != 0) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->item_empty[ic & 1u]);
+    }
+    if (!I.valid || *reinterpret_cast<volatile int*>(&ctl->abort_flag)) break;
 
     if (warp == 0 || warp == pf::kVWarp) {
       // ------------------------------------------------------- producers (TMA): warp 0 q and K,
       // warp 6 V.  Two issuing warps double the rate at which tile copies enter the TMA unit.
+      // The q tile of an item goes in once the S MMAs of the item before are done with theirs.
       const bool k_side = warp == 0;
-      if (!k_side && lane == 0) ctl->item[(ic + 1) & 1u] = claim_item(p, total);  // the next
-      if (k_side && lane == 0) {
+      bool ok = !k_side || ic == 0 || wait(&ctl->q_empty, (ic - 1) & 1u);
+      if (ok && k_side && lane == 0) {
         mbar_arrive_expect_tx(&ctl->q_full, pf::kTile);
         tma_load_3d(smem + pf::kQ, &qmap, 0, I.h * G, I.t0, &ctl->q_full);
         tma_load_3d(smem + pf::kQ + pf::kHalf, &qmap, 64, I.h * G, I.t0, &ctl->q_full);
       }
-      if (k_side) ++qiss;
+      if (ok && k_side) ++qiss;
       // Block-table entries are read 32 at a time (lane l holds block 32 * grp + l) with the
       // next group prefetched, so no TMA issue waits on a dependent table load.
       const int32_t* trow = p.block_tables + static_cast<int64_t>(I.s) * p.max_blocks_per_seq;
@@ -267,7 +295,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       int tab_cur = tab_load(grp_cur);
       int tab_next = tab_load(grp_cur + 1);
       const int yrow0 = I.h * 2;  // 8-row group of (block 0, this kv head)
-      for (int jj = 0; jj < I.nj; ++jj) {
+      for (int jj = 0; ok && jj < I.nj; ++jj) {
         const int j = I.j0 + jj;
         const int grp = j >> 2;
         if (grp != grp_cur) {
@@ -295,7 +323,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         const int ycoord = (phys * p.num_kv_heads) * 2 + yrow0;
         const uint32_t g = tc + jj, st = g % pf::kStages;
         if (k_side) {
-          if (!wait(&ctl->k_empty[st], ((g / pf::kStages) & 1u) ^ 1u)) break;
+          if (!(ok = wait(&ctl->k_empty[st], ((g / pf::kStages) & 1u) ^ 1u))) break;
           if (lane == 0) {
             if (bytes) mbar_arrive_expect_tx(&ctl->k_full[st], bytes);
             else mbar_arrive(&ctl->k_full[st]);
@@ -309,9 +337,9 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                         0, ycoord, &ctl->k_full[st]);
           ++kiss;
         } else {
-          if (!wait(&ctl->v_empty[st], ((g / pf::kStages) & 1u) ^ 1u)) break;
+          if (!(ok = wait(&ctl->v_empty[st], ((g / pf::kStages) & 1u) ^ 1u))) break;
           if (lane == 0) {
-            // rows the MMA warp has to clear: keys past the last valid one, and bad blocks
+            // rows the P V issuer clears: keys past the last valid one, and bad blocks
             const int valid_end = min(I.L, I.nblk_tile * kBlockSize) - j * pf::kKeys;
             ctl->v_zero_from[st] = max(0, min(pf::kKeys, valid_end));
             ctl->v_bad[st] = badm;
@@ -325,6 +353,18 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           ++viss;
         }
       }
+      // warp 0 claims the next item into the other slot, once the other warps have read the
+      // item that was last there
+      if (k_side && ok) {
+        const uint32_t next = ic + 1;
+        if (next >= 2 && !wait(&ctl->item_empty[next & 1u], ((next >> 1) - 1) & 1u)) break;
+        if (lane == 0) {
+          ctl->item[next & 1u] = claim_item(p, total);
+          mbar_arrive(&ctl->item_full[next & 1u]);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
     } else if (warp == 1) {
       // ------------------------------------------------------------- S issuer -----------
       // S of slice jj into the S buffer once the softmax has read S of jj - 1 out of it.
@@ -350,12 +390,20 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         }
         __syncwarp();
       }
+      // the q tile is free for the next item once these S MMAs have run
+      if (ok && lane == 0) tc_commit(&ctl->q_empty);
+      __syncwarp();
     } else if (warp == pf::kPvWarp) {
       // ------------------------------------------------------------- P V issuer ---------
       // O += P V of slice jj once its V has landed (rows without a valid key cleared) and the
       // softmax has handed over its P.  A warp of its own, so that neither issuer's waits hold
       // back the other's MMAs.
       const uint32_t id_pv = idesc_bf16_f32(128, 128, true);
+      // O starts over once the softmax warps have read the last item's
+      if (ic > 0) {
+        if (!wait(&ctl->o_free, (ic - 1) & 1u)) break;
+        tc_fence_after();
+      }
       for (int jj = 0; jj < I.nj; ++jj) {
         const uint32_t g = tc + jj, st = g % pf::kStages, b = g % pf::kPBufs;
         if (!wait(&ctl->v_full[st], (g / pf::kStages) & 1u)) break;
@@ -565,17 +613,29 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       const bool split = I.ns > 1;
       const uint32_t g_last = tc + I.nj - 1;
       const int sw = half ? warp - 4 : warp - 2;  // softmax warp index 0..7
-      uint8_t* stage = smem + pf::kK + sw * (32 * kC * 4);
+      uint8_t* stage = smem + pf::kStage + sw * (32 * kC * 4);
       const bool have =
           ok && live && wait(&ctl->o_done[g_last % pf::kPBufs], (g_last / pf::kPBufs) & 1u);
-      if (have) {
+      // O may take the next item's P V once every softmax warp has read it.  A warp with no
+      // row of this item gets here without waiting on any reader of the item before, so it
+      // first waits for that item's phase to complete: its arrival must not count there.
+      auto release_o = [&] {
+        if (ic > 0 && !wait(&ctl->o_free, (ic - 1) & 1u)) return;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->o_free);
+      };
+      if (!have) {  // warp-uniform
+        release_o();
+      } else {
         tc_fence_after();
-        const float inv = (row_ok && l > 0.f) ? 1.f / l : 0.f;
         uint32_t o[kC];
 #pragma unroll
         for (int c = 0; c < kC / 32; ++c)
           tmem_ld32(tl + pf::kOCol + hc + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&o[c * 32]));
         tmem_wait_ld();
+        release_o();
+        const float inv = (row_ok && l > 0.f) ? 1.f / l : 0.f;
         const bool bf16 = p.out_bf16 && !split;   // partials are fp32
         if (split && half == 0 && row_ok)
           p.part_lse[(static_cast<int64_t>(I.t0 + tok) * p.num_q_heads + I.h * G + r % G) *
@@ -633,13 +693,10 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         if (!bf16) write_rows(std::integral_constant<int, kC / 4>());
         else write_rows(std::integral_constant<int, kC / 8>());
       }
-      fence_proxy_async_smem();  // generic accesses to the K stages before the next copies
-      tc_fence_before();
     }
     tc += I.nj;
     ++ic;
-    __syncthreads();
-    tc_fence_after();
+    if (*reinterpret_cast<volatile int*>(&ctl->abort_flag)) break;
   }
   // Exit, normal or after an expired wait: no copy may still be landing in shared memory and
   // no MMA may still be using tensor memory when the CTA ends.
