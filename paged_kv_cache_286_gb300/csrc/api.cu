@@ -411,13 +411,17 @@ pa_status pa_attention(const void* q, int32_t num_q_tokens, const void* k_cache,
   const int32_t G = num_q_heads / num_kv_heads;
   const bool use_prefill = pa::prefill_path_enabled(*cache, num_q_heads, num_kv_heads) &&
                            pa::routes_to_prefill(max_query_len, G);
+  // whole (block, kv head) tiles of bf16 head_dim 128 pools in one copy: the split-KV kernel's
+  // and the prefill tiles' loads
+  if (cache->cache_dtype == PA_BF16 && cache->head_dim == 128) {
+    if ((st = encode_pool_tile_map(&maps.k4, k_cache, *cache)) != PA_OK) return st;
+    if ((st = encode_pool_tile_map(&maps.v4, v_cache, *cache)) != PA_OK) return st;
+    maps.has_k4 = true;
+  }
   if (use_prefill) {
     if ((st = encode_q_map(&maps.q3, q, num_q_tokens, num_q_heads, head_dim, G)) != PA_OK)
       return st;
     maps.has_q3 = true;
-    if ((st = encode_pool_tile_map(&maps.k4, k_cache, *cache)) != PA_OK) return st;
-    if ((st = encode_pool_tile_map(&maps.v4, v_cache, *cache)) != PA_OK) return st;
-    maps.has_k4 = true;
   }
 
   pa::AttnArgs a{q, num_q_tokens, k_cache, v_cache, *cache, block_tables, max_blocks_per_seq,

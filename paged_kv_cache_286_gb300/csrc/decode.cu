@@ -339,6 +339,18 @@ struct DecodeCfg {
   static constexpr int kBoxCols = kFp8 ? 128 : 64;                  // elements per 128-B row
   static constexpr int kBoxes = D / kBoxCols;                       // TMA boxes per tile
   static constexpr int kBoxBytes = HPI * kBlockSize * 128;          // 16 HPI rows x 128 B
+  // bf16 head_dim 128: the whole (block, head) tile in one 4-D copy (the pool seen as 64
+  // columns x 8 rows x 2 column halves x 8-row groups), laid out [row group][half][8 rows]
+  // [128 B], so one SM's copy engine moves twice the bytes per copy of two 2-D boxes
+  static constexpr bool kTile4d = !kFp8 && D == 128;
+  // shared-memory byte offset of 16-byte chunk `chunk` of key row `row` of a tile (swizzled)
+  __device__ static uint32_t offset(int row, int chunk) {
+    const uint32_t sw = static_cast<uint32_t>(((chunk & 7) ^ (row & 7)) << 4);
+    if constexpr (kTile4d)
+      return (row >> 3) * 2048 + (chunk >> 3) * 1024 + (row & 7) * 128 + sw;
+    else
+      return (chunk >> 3) * kBoxBytes + row * 128 + sw;
+  }
   static constexpr int kStageBytes = 2 * kTileBytes;                // K tiles + V tiles
   static constexpr int kKSteps = D / 16;
   // consecutive kv heads of a block are consecutive rows of the pool, so one box of 16 HPI rows
@@ -494,10 +506,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (kFp8 && HPI > 1) ? 3 : 1)
           // expects its bytes but gets no copy, so that the bounded wait on it expires
           const bool skip = p.skip_copy && I.idx == 0 && warp == 0 && k == 0;
           if (!skip) {
+            if constexpr (C::kTile4d) {
+              const int y4 = (phys * p.num_kv_heads + I.h) * 2;  // its first 8-row group
+              tma_load_4d(kt, &kmap, 0, 0, 0, y4, bar);
+              tma_load_4d(vt, &vmap, 0, 0, 0, y4, bar);
+            } else {
 #pragma unroll
-            for (int bx = 0; bx < C::kBoxes; ++bx) {
-              tma_load_2d(kt + bx * C::kBoxBytes, &kmap, bx * C::kBoxCols, y, bar);
-              tma_load_2d(vt + bx * C::kBoxBytes, &vmap, bx * C::kBoxCols, y, bar);
+              for (int bx = 0; bx < C::kBoxes; ++bx) {
+                tma_load_2d(kt + bx * C::kBoxBytes, &kmap, bx * C::kBoxCols, y, bar);
+                tma_load_2d(vt + bx * C::kBoxBytes, &vmap, bx * C::kBoxCols, y, bar);
+              }
             }
           }
         } else {
@@ -599,8 +617,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (kFp8 && HPI > 1) ? 3 : 1)
 #pragma unroll
             for (int kk = 0; kk < D / 32; ++kk) {
               const int chunk = 4 * kk + (lane >> 3);  // 16-byte chunk = 8 d
-              const uint32_t addr = kbase + (chunk >> 3) * C::kBoxBytes + krow * 128 +
-                                    (((chunk & 7) ^ (krow & 7)) << 4);
+              const uint32_t addr = kbase + C::offset(krow, chunk);
               uint32_t b0, b1, b2, b3;
               ldsm_x4(addr, b0, b1, b2, b3);
               mma_bf16(sacc[nt], qa[2 * kk], b0, b1);
@@ -704,8 +721,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (kFp8 && HPI > 1) ? 3 : 1)
 #pragma unroll
           for (int j = 0; j < C::kKSteps; ++j) {
             const int chunk = 2 * j + ((lane >> 3) & 1);
-            const uint32_t addr = vbase + (chunk >> 3) * C::kBoxBytes + vrow * 128 +
-                                  (((chunk & 7) ^ (vrow & 7)) << 4);
+            const uint32_t addr = vbase + C::offset(vrow, chunk);
             uint32_t a[4];
             ldsm_x4_t(addr, a[0], a[1], a[2], a[3]);
             if (nvalid < kBlockSize) {
@@ -1114,9 +1130,9 @@ cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const PoolMa
   else if (fp8)
     e = rt2 ? run_decode<128, true, 4, 2>(a, ws, p, kmap, vmap, before, after)
             : run_decode<128, true, 4, 1>(a, ws, p, kmap, vmap, before, after);
-  else if (a.head_dim == 128)
-    e = rt2 ? run_decode<128, false, 3, 2>(a, ws, p, kmap, vmap, before, after)
-            : run_decode<128, false, 3, 1>(a, ws, p, kmap, vmap, before, after);
+  else if (a.head_dim == 128)  // whole-tile 4-D copies
+    e = rt2 ? run_decode<128, false, 3, 2>(a, ws, p, maps.k4, maps.v4, before, after)
+            : run_decode<128, false, 3, 1>(a, ws, p, maps.k4, maps.v4, before, after);
   else
     e = rt2 ? run_decode<64, false, 4, 2>(a, ws, p, kmap, vmap, before, after)
             : run_decode<64, false, 4, 1>(a, ws, p, kmap, vmap, before, after);
