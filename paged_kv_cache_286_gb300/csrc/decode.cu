@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
   constexpr int kN = 4;      // decode items, prefill items, merge rows, runs with prefill items
   constexpr int kSortMax = 2048;  // runs the plan orders by length (more: sequence order)
   __shared__ int warp_sums[32][kN];
-  __shared__ int sort_key[kSortMax], sort_val[kSortMax];
+  __shared__ int sort_key[kSortMax], sort_val[kSortMax], sort_cnt[kSortMax];
   __shared__ int carry_s[kN];
   __shared__ float red_f[32][3];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -203,7 +203,16 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
     if (s < p.num_seqs) {
       p.item_start[s] = excl[0];
       p.merge_start[s] = excl[2];
-      if (cnt[3]) p.pf_order[excl[3]] = s;  // runs with prefill items, in sequence order
+      if (cnt[3]) {  // runs with prefill items, in sequence order
+        p.pf_order[excl[3]] = s;
+        if (excl[3] < kSortMax) {  // with their sort key and item count, for the ordering
+          const int n = p.qsl[s + 1] - p.qsl[s];
+          const int L = p.context_lens[s];
+          sort_key[excl[3]] = ceil_div((L - 1) / 128 + 1, prefill_splits(n, L, p.group, p.pmax));
+          sort_val[excl[3]] = s;
+          sort_cnt[excl[3]] = cnt[1];
+        }
+      }
     }
     __syncthreads();
     if (tid == 1023)
@@ -215,17 +224,13 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
   // so that the CTAs taking items from the counter end close together.  A bitonic sort in
   // shared memory, padded to a power of two with entries that sort last.
   const int R = carry_s[3];
-  auto longest_item = [&](int s) {
-    const int n = p.qsl[s + 1] - p.qsl[s];
-    const int L = p.context_lens[s];
-    return ceil_div((L - 1) / 128 + 1, prefill_splits(n, L, p.group, p.pmax));
-  };
   if (R > 1 && R <= kSortMax) {
     int n2 = 2;
     while (n2 < R) n2 <<= 1;
-    for (int i = tid; i < n2; i += 1024) {
-      sort_key[i] = i < R ? longest_item(p.pf_order[i]) : -1;
-      sort_val[i] = i < R ? p.pf_order[i] : INT_MAX;
+    for (int i = R + tid; i < n2; i += 1024) {
+      sort_key[i] = -1;
+      sort_val[i] = INT_MAX;
+      sort_cnt[i] = 0;
     }
     __syncthreads();
     for (int k = 2; k <= n2; k <<= 1)
@@ -237,10 +242,13 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
             const bool a_first = ka > kb || (ka == kb && va < vb);
             const bool b_first = kb > ka || (kb == ka && vb < va);
             if ((i & k) == 0 ? b_first : a_first) {
+              const int ca = sort_cnt[i];
               sort_key[i] = kb;
               sort_key[ixj] = ka;
               sort_val[i] = vb;
               sort_val[ixj] = va;
+              sort_cnt[i] = sort_cnt[ixj];
+              sort_cnt[ixj] = ca;
             }
           }
         }
@@ -255,7 +263,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
     for (int base = 0; base < R; base += 1024) {
       const int r = base + tid;
       int c = 0;
-      if (r < R) {
+      if (r < R && R <= kSortMax) {
+        c = sort_cnt[r];
+      } else if (r < R) {
         const int s = p.pf_order[r];
         c = prefill_items_of(p, p.qsl[s + 1] - p.qsl[s], p.context_lens[s]);
       }
@@ -297,32 +307,44 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
     red_f[warp][2] = dec_bytes;
   }
   __syncthreads();
+  float w_pf = 0.f, longest = 0.f, bytes = 0.f;
+  for (int i = 0; i < 32; ++i) {
+    w_pf += red_f[i][0];
+    longest = fmaxf(longest, red_f[i][1]);
+    bytes += red_f[i][2];
+  }
+  // SMs for the prefill tiles: the P that minimises the later of the two kernels' ends, the
+  // prefill taking max(work / P, longest item) and the split-KV kernel streaming its bytes on
+  // the other SMs (capped by the chip's HBM rate); the smallest P within 0.1 % of the best.
+  // Thread P - 1 evaluates P.
+  const int items = carry_s[1];
+  const int pmax = max(1, min(p.sms, items));
+  const bool search = bytes > 0.f && items > 0;
+  const int P = tid + 1;
+  float t = CUDART_INF_F;
+  if (search && P <= pmax) {
+    const float tp = fmaxf(w_pf / P, longest);
+    const float rate = fminf(kHbmBytesPerUs, float(p.sms - P) * kDecodeSmBytesPerUs);
+    t = fmaxf(tp, rate > 0.f ? bytes / rate : CUDART_INF_F);
+  }
+  __shared__ float red_t[32];
+  __shared__ int red_p[32];
+  float tm = t;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) tm = fminf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
+  if (lane == 0) red_t[warp] = tm;
+  __syncthreads();
+  tm = red_t[0];
+  for (int i = 1; i < 32; ++i) tm = fminf(tm, red_t[i]);
+  int cand = (search && P <= pmax && t <= tm * 1.001f) ? P : INT_MAX;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
+  if (lane == 0) red_p[warp] = cand;
+  __syncthreads();
   if (tid == 0) {
-    float w_pf = 0.f, longest = 0.f, bytes = 0.f;
-    for (int i = 0; i < 32; ++i) {
-      w_pf += red_f[i][0];
-      longest = fmaxf(longest, red_f[i][1]);
-      bytes += red_f[i][2];
-    }
-    // SMs for the prefill tiles: the P that minimises the later of the two kernels' ends,
-    // the prefill taking max(work / P, longest item) and the split-KV kernel streaming its
-    // bytes on the other SMs (capped by the chip's HBM rate)
-    const int items = carry_s[1];
-    const int pmax = max(1, min(p.sms, items));
-    int best_p = pmax;
-    if (bytes > 0.f && items > 0) {
-      float best = CUDART_INF_F;
-      for (int P = 1; P <= pmax; ++P) {
-        const float tp = fmaxf(w_pf / P, longest);
-        const float rate = fminf(kHbmBytesPerUs, float(p.sms - P) * kDecodeSmBytesPerUs);
-        const float td = rate > 0.f ? bytes / rate : CUDART_INF_F;
-        const float t = fmaxf(tp, td);
-        if (t < best * 0.999f) {
-          best = t;
-          best_p = P;
-        }
-      }
-    }
+    int best_p = INT_MAX;
+    for (int i = 0; i < 32; ++i) best_p = min(best_p, red_p[i]);
+    if (best_p == INT_MAX) best_p = pmax;
     p.item_start[p.num_seqs] = carry_s[0];
     p.merge_start[p.num_seqs] = carry_s[2];
     p.hdr->decode_counter = 0;
