@@ -3,15 +3,16 @@ memory (for example code running under a memory manager that owns the whole devi
 that must not grow its footprint after start-up).  It keeps its scratch in an array built into
 the library instead of a caller workspace.
 
-The GPU test calls it through the C ABI twice in a row, on two different steps (the second one
-smaller, so that stale scratch from the first call would show), and compares each output with
-the workspace-taking pa_attention on the same inputs, within the parity tolerance.  This file
-is named so that pytest collects it last.
+The GPU test calls it through the C ABI three times in a row, on different steps (split-KV
+with a merge, chunked-prefill tiles, and a smaller step last, so that stale scratch from the
+calls before would show), and checks each output against the fp64 oracle within the parity
+tolerance, and bit for bit against the workspace-taking pa_attention on the same inputs (the
+same kernels, with their scratch elsewhere).  This file is named so that pytest collects it
+last.
 """
 
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
@@ -40,22 +41,28 @@ def _call_noalloc(lib, d, error_word):
 
 
 @pytest.mark.gpu
-def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row():
+def test_noalloc_matches_the_oracle_on_three_calls_in_a_row():
     import gpu_harness as h
+    from oracle import run_step
     _l, lib = _lib()
-    first = make_workload([9000, 300, 17], [1, 1, 1], num_q_heads=32, num_kv_heads=8,
-                          head_dim=128, seed=41, pool_fill="nan")       # split-KV + merge path
-    second = make_config(1, pool_fill="nan")                             # smaller, no split
+    steps = [
+        make_workload([9000, 300, 17], [1, 1, 1], num_q_heads=32, num_kv_heads=8,
+                      head_dim=128, seed=41, pool_fill="nan"),       # split-KV + merge path
+        make_workload([600, 90, 2000], [130, 1, 1], num_q_heads=32, num_kv_heads=8,
+                      head_dim=128, seed=43, pool_fill="nan"),       # prefill tiles + decode
+        make_config(1, pool_fill="nan"),                             # smaller, no split
+    ]
     error_word = torch.full((1,), 0xFFFF, dtype=torch.int32, device="cuda")
-    for w in (first, second):
-        d, ref = h.run_gpu(w)                  # pa_attention with a caller workspace
-        ref = ref.clone()
+    for w in steps:
+        d, ws_out = h.run_gpu(w)               # pa_attention with a caller workspace
+        ws_out = ws_out.clone()
         st, out = _call_noalloc(lib, d, error_word)
         assert st == _l.PA_OK, lib.pa_last_error_string().decode()
         torch.cuda.synchronize()
         assert int(error_word.item()) == 0
-        diff = (out - ref).abs().max().item()
-        assert np.isfinite(diff) and diff <= h.tolerance(w), diff
+        _, _, ref = run_step(w)
+        h.assert_close_to_oracle(w, out, ref)
+        assert torch.equal(out, ws_out), "noalloc and workspace entry points differ"
 
 
 def test_noalloc_rejects_steps_beyond_its_scratch():
