@@ -510,17 +510,13 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         for (int i = 0; i < 8; ++i) mx[i] = -CUDART_INF_F;
         if (__all_sync(0xffffffffu, kmax >= kC - 1)) {  // warp-uniform branch
 #pragma unroll
-          for (int i = 0; i < kC; ++i) {
-            x[i] = __uint_as_float(sv[i]);
-            mx[i & 7] = fmaxf(mx[i & 7], x[i]);
-          }
+          for (int i = 0; i < kC; ++i) x[i] = __uint_as_float(sv[i]);
         } else {
 #pragma unroll
-          for (int i = 0; i < kC; ++i) {
-            x[i] = (i <= kmax) ? __uint_as_float(sv[i]) : -CUDART_INF_F;
-            mx[i & 7] = fmaxf(mx[i & 7], x[i]);
-          }
+          for (int i = 0; i < kC; ++i) x[i] = (i <= kmax) ? __uint_as_float(sv[i]) : -CUDART_INF_F;
         }
+#pragma unroll
+        for (int i = 0; i < kC; i += 2) mx[(i >> 1) & 7] = fmax3(mx[(i >> 1) & 7], x[i], x[i + 1]);
         float mt;
         if (!(ok = exchange(fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))),
@@ -550,30 +546,41 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         // columns 0..31 and lo parts into 32..63.  The split is by truncation, on the integer
         // pipes: hi keeps the upper 16 bits of p, lo = p - hi exactly in fp32, and lo is
         // truncated in turn, so hi + lo = p within 2^-14 relative.
+        // The pairs of keys go through Blackwell's two-wide fp32 instructions (the scale-and-shift,
+        // the row sums, the lo parts), each lane rounded as the scalar one would be.
         const uint32_t p_cols = tl + pf::kPCol + b * 128u + hc;
-        float rsum[8];
+        const f32x2 sl2 = f2_pack(p.score_log2, p.score_log2), mn2 = f2_pack(-m_new, -m_new);
+        f32x2 rsum[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) rsum[i] = 0.f;
+        for (int i = 0; i < 4; ++i) rsum[i] = f2_pack(0.f, 0.f);
 #pragma unroll
         for (int c = 0; c < kC / 32; ++c) {
           uint32_t hi[16], lo[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float p0 = fast_exp2(fmaf(x[c * 32 + 2 * e], p.score_log2, -m_new));
-            const float p1 = fast_exp2(fmaf(x[c * 32 + 2 * e + 1], p.score_log2, -m_new));
-            rsum[e & 7] += p0 + p1;
+            float a0, a1;
+            f2_unpack(f2_fma(f2_pack(x[c * 32 + 2 * e], x[c * 32 + 2 * e + 1]), sl2, mn2), a0, a1);
+            const float p0 = fast_exp2(a0), p1 = fast_exp2(a1);
+            const f32x2 pp = f2_pack(p0, p1);
+            rsum[e & 3] = f2_add(rsum[e & 3], pp);
             const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
             hi[e] = prmt(b0, b1, 0x7632u);
-            const float l0 = p0 - __uint_as_float(b0 & 0xffff0000u);
-            const float l1 = p1 - __uint_as_float(b1 & 0xffff0000u);
+            float l0, l1;
+            f2_unpack(f2_sub(pp, f2_pack(__uint_as_float(b0 & 0xffff0000u),
+                                         __uint_as_float(b1 & 0xffff0000u))),
+                      l0, l1);
             lo[e] = prmt(__float_as_uint(l0), __float_as_uint(l1), 0x7632u);
           }
           const uint32_t pc = p_cols + (c >> 1) * 64 + (c & 1) * 16;
           tmem_st16(pc, hi);
           tmem_st16(pc + 32, lo);
         }
-        const float rs = ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3])) +
-                         ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
+        float rs0, rs1, rs2, rs3, rs4, rs5, rs6, rs7;
+        f2_unpack(rsum[0], rs0, rs1);
+        f2_unpack(rsum[1], rs2, rs3);
+        f2_unpack(rsum[2], rs4, rs5);
+        f2_unpack(rsum[3], rs6, rs7);
+        const float rs = ((rs0 + rs1) + (rs2 + rs3)) + ((rs4 + rs5) + (rs6 + rs7));
         l = l * alpha + rs;
         if (__any_sync(0xffffffffu, rescale)) {
           // O may be rescaled only once the previous P V has landed in it (a rescale needs a
