@@ -29,7 +29,7 @@ struct WsHeader {
 // and MMAs, and its output); the HBM bytes per microsecond one SM's split-KV CTAs stream; and
 // the chip's HBM bytes per microsecond.
 constexpr float kTileSliceUs = 1.4f;
-constexpr float kTileItemUs = 6.5f;
+constexpr float kTileItemUs = 4.5f;
 constexpr float kDecodeSmBytesPerUs = 7.5e4f;
 constexpr float kHbmBytesPerUs = 6.7e6f;
 
