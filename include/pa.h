@@ -147,7 +147,7 @@ size_t pa_attention_workspace_size(int32_t num_seqs, int32_t num_q_tokens, int32
  * log2(e)-prescaled logits.
  * Kernels: every kernel of the call runs on `stream`, each launched early (programmatic
  * dependent launch) and waiting for what it reads: a plan, then, with a bf16 pool of head_dim
- * 128 and query runs of more than 16 tokens or more than 16 (token x q head) rows, the
+ * 128 or 64 and query runs of more than 16 tokens or more than 16 (token x q head) rows, the
  * tensor-core prefill tiles on the part of the SMs the plan gives them, the split-KV kernel on
  * the rest, and the merge of split sequences.  Work enqueued on `stream` after the call sees
  * all of it complete.  The call records no event and creates no stream, so it can be captured
@@ -216,7 +216,7 @@ void pa_set_kernel_timing_events(void* before, void* after);
 
 /* Benchmark hook, like pa_set_kernel_timing_events, for the tensor-core prefill-tile kernel
  * (launched only by steps that hold runs of more than 16 tokens or 16 token x head rows over a
- * bf16 pool with head_dim 128).  Pass NULLs to stop. */
+ * bf16 pool with head_dim 128 or 64).  Pass NULLs to stop. */
 void pa_set_prefill_timing_events(void* before, void* after);
 
 /* Benchmark hook that times kernels while they overlap: when `device_buffer` is non-NULL

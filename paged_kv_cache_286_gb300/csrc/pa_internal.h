@@ -99,7 +99,7 @@ cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const pa_cache_desc
                                cudaStream_t stream);
 
 // True when chunks with more than kDecodeMaxQuery queries run on the tcgen05 tile kernel
-// (bf16 pool, head_dim 128, GQA group dividing 128); otherwise every sequence takes the
+// (bf16 pool, head_dim 128 or 64, GQA group dividing 128); otherwise every sequence takes the
 // split-KV kernel.
 // Kv heads per split-KV work item (1 or 2) for a step of this shape; the pool's tensor maps
 // then take boxes of 16 x that many rows.

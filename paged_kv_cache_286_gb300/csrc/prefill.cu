@@ -76,7 +76,6 @@ constexpr int kStages = 2;   // K and V ring depth
 constexpr int kPBufs = 2;    // P buffers in TMEM, after the S buffer
 constexpr int kHalf = 16384;  // one 64-column half of the q tile
 constexpr int kTile = 32768;  // 128 x 128 bf16
-constexpr int kBlockBytes = 4096;  // one (block, kv head) tile of a K or V stage
 constexpr int kQ = 0, kK = kTile, kV = kK + kStages * kTile;
 constexpr int kStage = kV + kStages * kTile;  // the epilogue's staging of the softmax warps' rows
 constexpr int kStageBytes = 65536;
@@ -179,10 +178,14 @@ __device__ __forceinline__ PfItem claim_item(const PrefillParams& p, int total) 
   return it;
 }
 
+template <int D>
 __global__ void __launch_bounds__(pf::kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  constexpr int kBlk = 32 * D;   // bytes of one (block, kv head) tile
+  constexpr int kOC = D / 2;     // O columns of a softmax thread
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -279,9 +282,10 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       const bool k_side = warp == 0;
       bool ok = !k_side || ic == 0 || wait(&ctl->q_empty, (ic - 1) & 1u);
       if (ok && k_side && lane == 0) {
-        mbar_arrive_expect_tx(&ctl->q_full, pf::kTile);
+        mbar_arrive_expect_tx(&ctl->q_full, pf::kRows * D * 2);
         tma_load_3d(smem + pf::kQ, &qmap, 0, I.h * G, I.t0, &ctl->q_full);
-        tma_load_3d(smem + pf::kQ + pf::kHalf, &qmap, 64, I.h * G, I.t0, &ctl->q_full);
+        if constexpr (D == 128)
+          tma_load_3d(smem + pf::kQ + pf::kHalf, &qmap, 64, I.h * G, I.t0, &ctl->q_full);
       }
       if (ok && k_side) ++qiss;
       // Block-table entries are read 32 at a time (lane l holds block 32 * grp + l) with the
@@ -295,6 +299,13 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       int tab_cur = tab_load(grp_cur);
       int tab_next = tab_load(grp_cur + 1);
       const int yrow0 = I.h * 2;  // 8-row group of (block 0, this kv head)
+      // this lane's (block, kv head) tile of a slice into its place in a stage: one 4-D copy
+      // for head_dim 128 (the whole tile), one 2-D box of 16 rows x 128 B for 64
+      auto tile_copy = [&](int stage_off, const CUtensorMap* map, int group, uint64_t* bar) {
+        uint8_t* dst = smem + stage_off + lane * kBlk;
+        if constexpr (D == 128) tma_load_4d(dst, map, 0, 0, 0, group, bar);
+        else tma_load_2d(dst, map, 0, group * 8, bar);
+      };
       for (int jj = 0; ok && jj < I.nj; ++jj) {
         const int j = I.j0 + jj;
         const int grp = j >> 2;
@@ -319,7 +330,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         }
         const uint32_t okm = __ballot_sync(0xffffffffu, phys >= 0);
         const uint32_t badm = __ballot_sync(0xffffffffu, bad);
-        const uint32_t bytes = __popc(okm) * static_cast<uint32_t>(pf::kBlockBytes);
+        const uint32_t bytes = __popc(okm) * static_cast<uint32_t>(kBlk);
         const int ycoord = (phys * p.num_kv_heads) * 2 + yrow0;
         const uint32_t g = tc + jj, st = g % pf::kStages;
         if (k_side) {
@@ -332,9 +343,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           // test hook: lane 0's copy of the first slice of the first item claimed is left
           // out (its bytes are still expected), so that the bounded waits on that stage expire
           const bool skip = p.skip_copy && I.first && jj == 0 && lane == 0;
-          if (phys >= 0 && !skip)
-            tma_load_4d(smem + pf::kK + st * pf::kTile + lane * pf::kBlockBytes, &kmap, 0, 0,
-                        0, ycoord, &ctl->k_full[st]);
+          if (phys >= 0 && !skip) tile_copy(pf::kK + st * pf::kTile, &kmap, ycoord, &ctl->k_full[st]);
           ++kiss;
         } else {
           if (!(ok = wait(&ctl->v_empty[st], ((g / pf::kStages) & 1u) ^ 1u))) break;
@@ -347,9 +356,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             else mbar_arrive(&ctl->v_full[st]);
           }
           __syncwarp();
-          if (phys >= 0)
-            tma_load_4d(smem + pf::kV + st * pf::kTile + lane * pf::kBlockBytes, &vmap, 0, 0,
-                        0, ycoord, &ctl->v_full[st]);
+          if (phys >= 0) tile_copy(pf::kV + st * pf::kTile, &vmap, ycoord, &ctl->v_full[st]);
           ++viss;
         }
       }
@@ -379,11 +386,13 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         if (lane == 0) {
           const uint32_t k_addr = smem_u32(smem + pf::kK + st * pf::kTile);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
+          for (int ks = 0; ks < D / 16; ++ks) {
+            // 64-column halves of q 16 KiB apart; of a K block 1 KiB apart (head_dim 128: 8-key
+            // groups 2 KiB apart), or one half (64: 8-key groups 1 KiB apart)
             const uint32_t qa = q_addr + (ks >> 2) * pf::kHalf + (ks & 3) * 32;
             const uint32_t kb = k_addr + (ks >> 2) * 1024 + (ks & 3) * 32;
             tc_mma_bf16(tmem + pf::kSCol, smem_desc_sw128(qa, 16, 1024),
-                        smem_desc_sw128(kb, 16, 2048), id_s, ks > 0);
+                        smem_desc_sw128(kb, 16, D == 128 ? 2048 : 1024), id_s, ks > 0);
           }
           tc_commit(&ctl->s_full);
           tc_commit(&ctl->k_empty[st]);
@@ -398,7 +407,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       // O += P V of slice jj once its V has landed (rows without a valid key cleared) and the
       // softmax has handed over its P.  A warp of its own, so that neither issuer's waits hold
       // back the other's MMAs.
-      const uint32_t id_pv = idesc_bf16_f32(128, 128, true);
+      const uint32_t id_pv = idesc_bf16_f32(128, D, true);
       // O starts over once the softmax warps have read the last item's
       if (ic > 0) {
         if (!wait(&ctl->o_free, (ic - 1) & 1u)) break;
@@ -411,13 +420,14 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         const int zf = ctl->v_zero_from[st];
         const uint32_t badm = ctl->v_bad[st];
         if (zf < pf::kKeys || badm) {
-          // clear the 128-byte rows (both column halves) of keys that hold no valid value;
+          // clear the 128-byte rows (every column half) of keys that hold no valid value;
           // key kk of the slice: block kk / 16, row group (kk / 8) % 2, row kk % 8
-          for (int e = lane; e < pf::kKeys * 2 * 8; e += 32) {
-            const int key = e >> 4, half = (e >> 3) & 1, c16 = e & 7;
+          constexpr int kHalves = D / 64;
+          for (int e = lane; e < pf::kKeys * kHalves * 8; e += 32) {
+            const int key = e / (kHalves * 8), half = (e >> 3) % kHalves, c16 = e & 7;
             if (key >= zf || ((badm >> (key >> 4)) & 1u))
-              *reinterpret_cast<uint4*>(vt + (key >> 3) * 2048 + half * 1024 + (key & 7) * 128 +
-                                        c16 * 16) = make_uint4(0u, 0u, 0u, 0u);
+              *reinterpret_cast<uint4*>(vt + (key >> 3) * (kHalves * 1024) + half * 1024 +
+                                        (key & 7) * 128 + c16 * 16) = make_uint4(0u, 0u, 0u, 0u);
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -428,20 +438,20 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           const uint32_t v_addr = smem_u32(vt);
           // P of keys 16 ks .. 16 ks + 15: the hi parts of keys 0-63 in columns 0-31 of the
           // buffer and their lo parts in 32-63; keys 64-127 the same in columns 64-127.  V of
-          // those keys: block ks of the stage, MN-major (the column halves 1 KiB apart, 8-key
-          // groups 2 KiB apart).
+          // those keys: block ks of the stage, MN-major (head_dim 128: the column halves 1 KiB
+          // apart, 8-key groups 2 KiB apart; 64: one half, 8-key groups 1 KiB apart).
           auto p_col = [&](int ks) {
             return tmem + pf::kPCol + b * 128u + (ks >> 2) * 64u + (ks & 3) * 8u;
           };
+          auto v_desc = [&](int ks) {
+            return smem_desc_sw128(v_addr + ks * kBlk, 1024, D == 128 ? 2048 : 1024);
+          };
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            tc_mma_bf16_ts(tmem + pf::kOCol, p_col(ks),
-                           smem_desc_sw128(v_addr + ks * 4096, 1024, 2048), id_pv,
-                           jj > 0 || ks > 0);
+            tc_mma_bf16_ts(tmem + pf::kOCol, p_col(ks), v_desc(ks), id_pv, jj > 0 || ks > 0);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            tc_mma_bf16_ts(tmem + pf::kOCol, p_col(ks) + 32u,
-                           smem_desc_sw128(v_addr + ks * 4096, 1024, 2048), id_pv, true);
+            tc_mma_bf16_ts(tmem + pf::kOCol, p_col(ks) + 32u, v_desc(ks), id_pv, true);
           tc_commit(&ctl->o_done[b]);
           tc_commit(&ctl->v_empty[st]);
         }
@@ -457,7 +467,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       const bool row_ok = tok < I.ntok;
       const int row_pos = I.pos0 + tok;
       const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-      const uint32_t hc = half * 64u;      // first S / P / O column of this thread
+      const uint32_t hc = half * 64u;      // first S / P column of this thread
+      const uint32_t oc = half * kOC;      // and its first O column
       uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + pf::kXBar) + quarter;
       // Combine v with the other half of the row (max, or sum): both threads fold v into the
       // row's slot, the two warps meet at the pair's barrier (lane 0 of each arrives once the
@@ -588,17 +599,17 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           if (!(ok = wait(&ctl->o_done[(g - 1) % pf::kPBufs], ((g - 1) / pf::kPBufs) & 1u)))
             break;
           tc_fence_after();
-          uint32_t o[kC];
+          uint32_t o[kOC];
 #pragma unroll
-          for (int c = 0; c < kC / 32; ++c)
-            tmem_ld32(tl + pf::kOCol + hc + c * 32,
+          for (int c = 0; c < kOC / 32; ++c)
+            tmem_ld32(tl + pf::kOCol + oc + c * 32,
                       *reinterpret_cast<uint32_t(*)[32]>(&o[c * 32]));
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < kC; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          for (int i = 0; i < kOC; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
 #pragma unroll
-          for (int c = 0; c < kC / 32; ++c)
-            tmem_st32(tl + pf::kOCol + hc + c * 32,
+          for (int c = 0; c < kOC / 32; ++c)
+            tmem_st32(tl + pf::kOCol + oc + c * 32,
                       *reinterpret_cast<uint32_t(*)[32]>(&o[c * 32]));
         }
         tmem_wait_st();
@@ -620,7 +631,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       const bool split = I.ns > 1;
       const uint32_t g_last = tc + I.nj - 1;
       const int sw = half ? warp - 4 : warp - 2;  // softmax warp index 0..7
-      uint8_t* stage = smem + pf::kStage + sw * (32 * kC * 4);
+      uint8_t* stage = smem + pf::kStage + sw * (32 * kOC * 4);
       const bool have =
           ok && live && wait(&ctl->o_done[g_last % pf::kPBufs], (g_last / pf::kPBufs) & 1u);
       // O may take the next item's P V once every softmax warp has read it.  A warp with no
@@ -636,10 +647,10 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         release_o();
       } else {
         tc_fence_after();
-        uint32_t o[kC];
+        uint32_t o[kOC];
 #pragma unroll
-        for (int c = 0; c < kC / 32; ++c)
-          tmem_ld32(tl + pf::kOCol + hc + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&o[c * 32]));
+        for (int c = 0; c < kOC / 32; ++c)
+          tmem_ld32(tl + pf::kOCol + oc + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&o[c * 32]));
         tmem_wait_ld();
         release_o();
         const float inv = (row_ok && l > 0.f) ? 1.f / l : 0.f;
@@ -649,7 +660,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                          p.pmax + I.k] =
               (seen && l > 0.f) ? m_used + __log2f(l) : -CUDART_INF_F;
         if (!bf16) {
-          constexpr int CH = kC / 4;   // 16-byte chunks of the thread's row part
+          constexpr int CH = kOC / 4;   // 16-byte chunks of the thread's row part
 #pragma unroll
           for (int c = 0; c < CH; ++c)
             *reinterpret_cast<uint4*>(stage + lane * CH * 16 + ((c ^ lane) & (CH - 1)) * 16) =
@@ -658,7 +669,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                            __float_as_uint(__uint_as_float(o[4 * c + 2]) * inv),
                            __float_as_uint(__uint_as_float(o[4 * c + 3]) * inv));
         } else {
-          constexpr int CH = kC / 8;
+          constexpr int CH = kOC / 8;
 #pragma unroll
           for (int c = 0; c < CH; ++c)
             *reinterpret_cast<uint4*>(stage + lane * CH * 16 + ((c ^ lane) & (CH - 1)) * 16) =
@@ -677,10 +688,10 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         const int64_t orow = static_cast<int64_t>(I.t0 + tok) * p.num_q_heads + I.h * G + r % G;
         uint8_t* my_dst =
             !row_ok ? nullptr
-            : split ? reinterpret_cast<uint8_t*>(p.part_o + (orow * p.pmax + I.k) * 128 + hc)
+            : split ? reinterpret_cast<uint8_t*>(p.part_o + (orow * p.pmax + I.k) * D + oc)
             : bf16  ? reinterpret_cast<uint8_t*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
-                                                 orow * 128 + hc)
-                    : reinterpret_cast<uint8_t*>(reinterpret_cast<float*>(p.out) + orow * 128 + hc);
+                                                 orow * D + oc)
+                    : reinterpret_cast<uint8_t*>(reinterpret_cast<float*>(p.out) + orow * D + oc);
         const uint32_t stage_s = smem_u32(stage);
         auto write_rows = [&](auto ch_tag) {
           constexpr int CH = decltype(ch_tag)::value;
@@ -697,8 +708,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             if (dst) *reinterpret_cast<uint4*>(dst + c * 16) = v;
           }
         };
-        if (!bf16) write_rows(std::integral_constant<int, kC / 4>());
-        else write_rows(std::integral_constant<int, kC / 8>());
+        if (!bf16) write_rows(std::integral_constant<int, kOC / 4>());
+        else write_rows(std::integral_constant<int, kOC / 8>());
       }
     }
     tc += I.nj;
@@ -732,10 +743,11 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
 
 namespace {
 
+template <int D>
 cudaError_t launch_prefill_grid(const AttnArgs& a, const PrefillParams& p, const CUtensorMap& qmap,
                                 const CUtensorMap& kmap, const CUtensorMap& vmap) {
   LaunchInfo li;
-  cudaError_t e = launch_info(prefill_kernel, pf::kThreads, pf::kSmemBytes, &li);
+  cudaError_t e = launch_info(prefill_kernel<D>, pf::kThreads, pf::kSmemBytes, &li);
   if (e != cudaSuccess) return e;
   // at most one CTA per SM (shared memory); the plan decides how many of them work
   const int64_t upper =
@@ -744,7 +756,7 @@ cudaError_t launch_prefill_grid(const AttnArgs& a, const PrefillParams& p, const
        a.num_seqs);
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(upper, li.sms));
   if (a.pf_before && a.pf_after) cudaEventRecord(a.pf_before, a.stream);
-  e = launch_dependent(prefill_kernel, dim3(static_cast<unsigned>(grid)), dim3(pf::kThreads),
+  e = launch_dependent(prefill_kernel<D>, dim3(static_cast<unsigned>(grid)), dim3(pf::kThreads),
                        pf::kSmemBytes, a.stream, qmap, kmap, vmap, p);
   if (a.pf_before && a.pf_after) cudaEventRecord(a.pf_after, a.stream);
   return e;
@@ -777,7 +789,9 @@ cudaError_t launch_prefill(const AttnArgs& a, const int32_t* item_start, const i
   p.part_lse = scratch.part_lse;
   p.part_o = scratch.part_o;
   p.pmax = scratch.pmax;
-  return launch_prefill_grid(a, p, maps.q3, maps.k4, maps.v4);
+  // head_dim 128: whole-tile 4-D copies; 64: the 2-D pool view, whose 16-row box is the tile
+  if (a.head_dim == 64) return launch_prefill_grid<64>(a, p, maps.q3, maps.k2, maps.v2);
+  return launch_prefill_grid<128>(a, p, maps.q3, maps.k4, maps.v4);
 }
 
 }  // namespace pa

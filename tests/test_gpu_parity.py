@@ -170,6 +170,18 @@ def test_prefill_chunks_bf16_output():
     _check_small(w, out_dtype=torch.bfloat16)
 
 
+@pytest.mark.parametrize("hq,hkv,out", [(8, 8, "f32"), (16, 4, "f32"), (32, 4, "f32"),
+                                         (16, 2, "f32"), (32, 4, "bf16")])
+def test_prefill_chunks_head_dim_64(hq, hkv, out):
+    """head_dim 64 chunks on the tensor-core tiles (one 64-column q half, 2 KiB block tiles by
+    2-D copies, 64 O columns): chunks with and without a cached prefix, a tile long enough to
+    be cut along the keys (7,000 keys: two splits, merged), a five-token verify run, and
+    decodes beside them; stale slots hold NaN patterns."""
+    w = make_workload([700, 17, 7000, 300, 90, 3000], [200, 17, 200, 5, 1, 1], num_q_heads=hq,
+                      num_kv_heads=hkv, head_dim=64, seed=hq * 5 + hkv, pool_fill="nan")
+    _check_small(w, torch.bfloat16 if out == "bf16" else torch.float32)
+
+
 def test_large_v_values_keep_their_precision():
     """V values far outside the N(0,1) range (+-65536, beyond what fp16 can hold, and 65280)
     in tensor-core tiles: P V stays exact (bf16 hi + lo parts of P against bf16 V), so the
