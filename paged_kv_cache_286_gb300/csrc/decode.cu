@@ -1065,8 +1065,9 @@ int decode_heads_per_item(const pa_cache_desc& c, int32_t num_q_heads, int32_t n
 
 bool prefill_path_enabled(const pa_cache_desc& c, int32_t num_q_heads, int32_t num_kv_heads) {
   const int G = num_q_heads / num_kv_heads;
-  return c.cache_dtype == PA_BF16 && (c.head_dim == 128 || c.head_dim == 64) && G >= 1 &&
-         G <= kRowsPerTile && 128 % G == 0;
+  const bool built = (c.cache_dtype == PA_BF16 && (c.head_dim == 128 || c.head_dim == 64)) ||
+                     (c.cache_dtype == PA_FP8_E4M3 && c.head_dim == 128);
+  return built && G >= 1 && G <= kRowsPerTile && 128 % G == 0;
 }
 
 cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const PoolMaps& maps,

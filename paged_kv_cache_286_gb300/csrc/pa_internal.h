@@ -99,8 +99,8 @@ cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const pa_cache_desc
                                cudaStream_t stream);
 
 // True when chunks with more than kDecodeMaxQuery queries run on the tcgen05 tile kernel
-// (bf16 pool, head_dim 128 or 64, GQA group dividing 128); otherwise every sequence takes the
-// split-KV kernel.
+// (bf16 pool of head_dim 128 or 64, or E4M3 of 128; GQA group dividing 128); otherwise every
+// sequence takes the split-KV kernel.
 // Kv heads per split-KV work item (1 or 2) for a step of this shape; the pool's tensor maps
 // then take boxes of 16 x that many rows.
 int decode_heads_per_item(const pa_cache_desc& c, int32_t num_q_heads, int32_t num_kv_heads,
@@ -149,7 +149,8 @@ struct PrefillParams {
   int32_t group;
   int32_t num_blocks;
   int32_t out_bf16;
-  float score_log2;
+  float score_log2;   // scale * log2(e) (* k_scale for E4M3 pools)
+  float v_out_scale;  // v_scale for E4M3 pools, else 1
   uint64_t wait_ns;   // limit of every bounded wait
   int32_t skip_copy;  // test hook: the first item claimed leaves out its first K copy
   uint64_t* span;     // benchmark hook: [first CTA start, last CTA end] in ns, or NULL

@@ -74,26 +74,40 @@ constexpr int kRows = 128;
 constexpr int kKeys = 128;
 constexpr int kStages = 2;   // K and V ring depth
 constexpr int kPBufs = 2;    // P buffers in TMEM, after the S buffer
-constexpr int kHalf = 16384;  // one 64-column half of the q tile
-constexpr int kTile = 32768;  // 128 x 128 bf16
-constexpr int kQ = 0, kK = kTile, kV = kK + kStages * kTile;
-constexpr int kStage = kV + kStages * kTile;  // the epilogue's staging of the softmax warps' rows
+constexpr int kHalf = 16384;  // one 64-column half of the q tile (bf16), or one E4M3 q part
 constexpr int kStageBytes = 65536;
-constexpr int kCtl = kStage + kStageBytes;    // control block (barriers, items, flags)
-constexpr int kXBar = kCtl + 384;           // 4 mbarriers: one per pair of softmax warps
-constexpr int kXSlot = kXBar + 32;          // 3 x 128 row slots of the pairs' exchanges
 constexpr int kXBufs = 3;
+// Shared memory, by the pool's element type: the q tile (bf16: two 64-column halves; E4M3 pools:
+// the bf16 tile lands there and becomes three E4M3 parts), the K and V rings (a stage is the 8
+// (block, kv head) tiles of 128 keys: 32 KiB bf16, 16 KiB E4M3), the epilogue's staging of the
+// softmax warps' rows, the control block, the row exchanges' mbarriers (one per lane quarter)
+// and slots.
+struct Layout {
+  int q_bytes, stage_stride, k, v, stage, ctl, xbar, xslot, smem;
+  __host__ __device__ constexpr Layout(bool fp8)
+      : q_bytes(fp8 ? 3 * kHalf : 2 * kHalf),
+        stage_stride(fp8 ? 16384 : 32768),
+        k(q_bytes),
+        v(k + kStages * stage_stride),
+        stage(v + kStages * stage_stride),
+        ctl(stage + kStageBytes),
+        xbar(ctl + 384),
+        xslot(xbar + 32),
+        smem(1024 + xslot + kXBufs * kRows * 4) {}
+};
+constexpr int kQ = 0;
 constexpr int kVWarp = 6;     // V producer (warp 0 loads q and K)
 constexpr int kPvWarp = 7;    // P V issuer (warp 1 issues S)
 // The softmax: warps 2-5 take keys 0-63 of their rows and warps 8-11 keys 64-127, and the
 // pairs exchange row sums and maxima through shared memory.
 constexpr int kThreads = 384;
 constexpr int kSoftmaxThreads = 256;
-constexpr int kSmemBytes = 1024 + kXSlot + kXBufs * kRows * 4;
+
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol = 0, kPCol = 128, kOCol = kPCol + kPBufs * 128;
 static_assert(kOCol + 128 == kTmemCols, "TMEM columns");
 constexpr float kRescaleLog2 = 8.f;
+constexpr float kRescaleLog2Fp8 = 0.5f;  // E4M3 P (times 2^8) stays under 2^8.5 < 448
 }  // namespace pf
 
 struct PfItem {
@@ -105,7 +119,7 @@ struct PfItem {
 struct PfCtl {
   uint64_t q_full, k_full[pf::kStages], k_empty[pf::kStages], v_full[pf::kStages],
       v_empty[pf::kStages], s_full, s_free, p_full[pf::kPBufs], o_done[pf::kPBufs], drain[2],
-      q_empty, o_free, item_full[2], item_empty[2];
+      q_empty, o_free, item_full[2], item_empty[2], q_ready;
   uint32_t tmem_base;
   int abort_flag;
   int v_zero_from[pf::kStages];
@@ -113,7 +127,8 @@ struct PfCtl {
   PfItem item[2];  // by the parity of the item count: warp 0 fills one while the other is read
 };
 static_assert(sizeof(PfCtl) <= 384, "control block too large");
-static_assert(pf::kSmemBytes <= 232448, "more shared memory than a CTA may have");
+static_assert(pf::Layout(false).smem <= 232448 && pf::Layout(true).smem <= 232448,
+              "more shared memory than a CTA may have");
 
 // Floats mapped to ints of the same order (an involution), so that integer atomicMax takes the
 // max of floats.  The empty slot INT_MIN is below every mapped float and reads as -0.0f.
@@ -178,18 +193,20 @@ __device__ __forceinline__ PfItem claim_item(const PrefillParams& p, int total) 
   return it;
 }
 
-template <int D>
+template <int D, bool kFp8>
 __global__ void __launch_bounds__(pf::kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
-  constexpr int kBlk = 32 * D;   // bytes of one (block, kv head) tile
+  static_assert(!kFp8 || D == 128, "E4M3 tiles have head_dim 128");
+  constexpr pf::Layout kL(kFp8);
+  constexpr int kBlk = 16 * D * (kFp8 ? 1 : 2);  // bytes of one (block, kv head) tile
   constexpr int kOC = D / 2;     // O columns of a softmax thread
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  PfCtl* ctl = reinterpret_cast<PfCtl*>(smem + pf::kCtl);
+  PfCtl* ctl = reinterpret_cast<PfCtl*>(smem + kL.ctl);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Launched right after the plan (programmatic dependent launch): wait for its items and SM
   // budget, let the split-KV kernel launch onto the SMs this kernel leaves, and end the CTAs
@@ -226,13 +243,14 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     // item before have read theirs (q_empty), and the P V issuer starts the next item's O once
     // the softmax warps have read the last one (o_free: one lane of each of the 8).
     mbar_init(&ctl->q_empty, 1);
+    mbar_init(&ctl->q_ready, pf::kSoftmaxThreads / 32);  // E4M3 pools: q parts written
     mbar_init(&ctl->o_free, pf::kSoftmaxThreads / 32);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl->item_full[i], 1);
       mbar_init(&ctl->item_empty[i], pf::kThreads / 32 - 1);
     }
     for (int q = 0; q < 4; ++q)
-        mbar_init(reinterpret_cast<uint64_t*>(smem + pf::kXBar) + q, 2);  // one lane a warp
+        mbar_init(reinterpret_cast<uint64_t*>(smem + kL.xbar) + q, 2);  // one lane a warp
     ctl->abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&qmap);
@@ -241,7 +259,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     ctl->item[0] = claim_item(p, total);
     mbar_arrive(&ctl->item_full[0]);
   }
-  int* xslot = reinterpret_cast<int*>(smem + pf::kXSlot);  // [kXBufs][kRows], split only
+  int* xslot = reinterpret_cast<int*>(smem + kL.xslot);  // [kXBufs][kRows]
   for (int i = tid; i < pf::kXBufs * pf::kRows; i += pf::kThreads) xslot[i] = INT_MIN;
   if (warp == 1) tmem_alloc(&ctl->tmem_base, pf::kTmemCols);
   tc_fence_before();
@@ -300,10 +318,10 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       int tab_next = tab_load(grp_cur + 1);
       const int yrow0 = I.h * 2;  // 8-row group of (block 0, this kv head)
       // this lane's (block, kv head) tile of a slice into its place in a stage: one 4-D copy
-      // for head_dim 128 (the whole tile), one 2-D box of 16 rows x 128 B for 64
+      // for bf16 head_dim 128 (the whole tile), one 2-D box of 16 rows x 128 B otherwise
       auto tile_copy = [&](int stage_off, const CUtensorMap* map, int group, uint64_t* bar) {
         uint8_t* dst = smem + stage_off + lane * kBlk;
-        if constexpr (D == 128) tma_load_4d(dst, map, 0, 0, 0, group, bar);
+        if constexpr (D == 128 && !kFp8) tma_load_4d(dst, map, 0, 0, 0, group, bar);
         else tma_load_2d(dst, map, 0, group * 8, bar);
       };
       for (int jj = 0; ok && jj < I.nj; ++jj) {
@@ -343,7 +361,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           // test hook: lane 0's copy of the first slice of the first item claimed is left
           // out (its bytes are still expected), so that the bounded waits on that stage expire
           const bool skip = p.skip_copy && I.first && jj == 0 && lane == 0;
-          if (phys >= 0 && !skip) tile_copy(pf::kK + st * pf::kTile, &kmap, ycoord, &ctl->k_full[st]);
+          if (phys >= 0 && !skip)
+            tile_copy(kL.k + st * kL.stage_stride, &kmap, ycoord, &ctl->k_full[st]);
           ++kiss;
         } else {
           if (!(ok = wait(&ctl->v_empty[st], ((g / pf::kStages) & 1u) ^ 1u))) break;
@@ -356,7 +375,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             else mbar_arrive(&ctl->v_full[st]);
           }
           __syncwarp();
-          if (phys >= 0) tile_copy(pf::kV + st * pf::kTile, &vmap, ycoord, &ctl->v_full[st]);
+          if (phys >= 0) tile_copy(kL.v + st * kL.stage_stride, &vmap, ycoord, &ctl->v_full[st]);
           ++viss;
         }
       }
@@ -375,16 +394,28 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     } else if (warp == 1) {
       // ------------------------------------------------------------- S issuer -----------
       // S of slice jj into the S buffer once the softmax has read S of jj - 1 out of it.
-      const uint32_t id_s = idesc_bf16_f32(128, 128, false);
+      const uint32_t id_s = kFp8 ? idesc_e4m3_f32(128, 128, false) : idesc_bf16_f32(128, 128, false);
       const uint32_t q_addr = smem_u32(smem + pf::kQ);
-      bool ok = wait(&ctl->q_full, ic & 1u);
+      // E4M3 pools: the softmax warps turn the bf16 q tile into three E4M3 parts first
+      bool ok = wait(kFp8 ? &ctl->q_ready : &ctl->q_full, ic & 1u);
       for (int jj = 0; ok && jj < I.nj; ++jj) {
         const uint32_t g = tc + jj, st = g % pf::kStages;
         if (g > 0 && !(ok = wait(&ctl->s_free, (g - 1) & 1u))) break;
         if (!(ok = wait(&ctl->k_full[st], (g / pf::kStages) & 1u))) break;
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t k_addr = smem_u32(smem + pf::kK + st * pf::kTile);
+          const uint32_t k_addr = smem_u32(smem + kL.k + st * kL.stage_stride);
+          if constexpr (kFp8) {
+            // S = (q_hi + q_mid + q_lo) K^T, 32 dims a step: q parts 16 KiB apart, K and q rows
+            // of 128 bytes (8-row groups 1 KiB apart)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+              for (int part = 0; part < 3; ++part)
+                tc_mma_f8(tmem + pf::kSCol,
+                          smem_desc_sw128(q_addr + part * pf::kHalf + ks * 32, 16, 1024),
+                          smem_desc_sw128(k_addr + ks * 32, 16, 1024), id_s, ks > 0 || part > 0);
+          } else {
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             // 64-column halves of q 16 KiB apart; of a K block 1 KiB apart (head_dim 128: 8-key
@@ -393,6 +424,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             const uint32_t kb = k_addr + (ks >> 2) * 1024 + (ks & 3) * 32;
             tc_mma_bf16(tmem + pf::kSCol, smem_desc_sw128(qa, 16, 1024),
                         smem_desc_sw128(kb, 16, D == 128 ? 2048 : 1024), id_s, ks > 0);
+          }
           }
           tc_commit(&ctl->s_full);
           tc_commit(&ctl->k_empty[st]);
@@ -407,7 +439,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       // O += P V of slice jj once its V has landed (rows without a valid key cleared) and the
       // softmax has handed over its P.  A warp of its own, so that neither issuer's waits hold
       // back the other's MMAs.
-      const uint32_t id_pv = idesc_bf16_f32(128, D, true);
+      const uint32_t id_pv = kFp8 ? idesc_e4m3_f32(128, D, true) : idesc_bf16_f32(128, D, true);
       // O starts over once the softmax warps have read the last item's
       if (ic > 0) {
         if (!wait(&ctl->o_free, (ic - 1) & 1u)) break;
@@ -416,13 +448,13 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       for (int jj = 0; jj < I.nj; ++jj) {
         const uint32_t g = tc + jj, st = g % pf::kStages, b = g % pf::kPBufs;
         if (!wait(&ctl->v_full[st], (g / pf::kStages) & 1u)) break;
-        uint8_t* vt = smem + pf::kV + st * pf::kTile;
+        uint8_t* vt = smem + kL.v + st * kL.stage_stride;
         const int zf = ctl->v_zero_from[st];
         const uint32_t badm = ctl->v_bad[st];
         if (zf < pf::kKeys || badm) {
           // clear the 128-byte rows (every column half) of keys that hold no valid value;
           // key kk of the slice: block kk / 16, row group (kk / 8) % 2, row kk % 8
-          constexpr int kHalves = D / 64;
+          constexpr int kHalves = kBlk / 2048;  // 128-byte column halves of a key's row
           for (int e = lane; e < pf::kKeys * kHalves * 8; e += 32) {
             const int key = e / (kHalves * 8), half = (e >> 3) % kHalves, c16 = e & 7;
             if (key >= zf || ((badm >> (key >> 4)) & 1u))
@@ -443,6 +475,18 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           auto p_col = [&](int ks) {
             return tmem + pf::kPCol + b * 128u + (ks >> 2) * 64u + (ks & 3) * 8u;
           };
+          if constexpr (kFp8) {
+            // P as E4M3 hi and lo parts, 4 keys a column: keys 32 ks .. 32 ks + 31 in columns
+            // 8 ks .. 8 ks + 7 (hi) and 32 + 8 ks .. (lo); V of those keys: blocks 2 ks and
+            // 2 ks + 1 of the stage, MN-major rows of 128 bytes (8-key groups 1 KiB apart)
+            const uint32_t pb = tmem + pf::kPCol + b * 128u;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint64_t vd = smem_desc_sw128(v_addr + ks * 2 * kBlk, 1024, 1024);
+              tc_mma_f8_ts(tmem + pf::kOCol, pb + ks * 8, vd, id_pv, jj > 0 || ks > 0);
+              tc_mma_f8_ts(tmem + pf::kOCol, pb + 32 + ks * 8, vd, id_pv, true);
+            }
+          } else {
           auto v_desc = [&](int ks) {
             return smem_desc_sw128(v_addr + ks * kBlk, 1024, D == 128 ? 2048 : 1024);
           };
@@ -452,6 +496,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
             tc_mma_bf16_ts(tmem + pf::kOCol, p_col(ks) + 32u, v_desc(ks), id_pv, true);
+          }
           tc_commit(&ctl->o_done[b]);
           tc_commit(&ctl->v_empty[st]);
         }
@@ -469,7 +514,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
       const uint32_t hc = half * 64u;      // first S / P column of this thread
       const uint32_t oc = half * kOC;      // and its first O column
-      uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + pf::kXBar) + quarter;
+      uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + kL.xbar) + quarter;
       // Combine v with the other half of the row (max, or sum): both threads fold v into the
       // row's slot, the two warps meet at the pair's barrier (lane 0 of each arrives once the
       // warp's updates are ordered before it) and read the slot; then the slot that the
@@ -492,12 +537,83 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       const bool live = __any_sync(0xffffffffu, row_ok);
       float m_used = 0.f, l = 0.f;
       bool seen = false;  // whether m_used comes from a visible key yet
+      bool ok = true;
+      // Scores of this row are multiplied by sl_row: scale * log2 e (* k_scale for E4M3),
+      // and for E4M3 by the row's q scale as well.
+      float sl_row = p.score_log2;
+      if constexpr (kFp8) {
+        // The bf16 q tile (two 64-column halves, each row 128 swizzled bytes) becomes three
+        // E4M3 parts of the same layout (one 128-byte row each, parts 16 KiB apart): q is
+        // scaled per row by 2^e, with the row's max magnitude in [128, 256); hi = e4m3(q 2^e),
+        // mid = e4m3 of the rest, lo = e4m3 of what is left, so q 2^e = hi + mid + lo to about
+        // 2^-12 of the row max.  This thread converts its half of the row; the two threads of a
+        // row agree on its max first, which also orders their reads of the bf16 halves before
+        // either writes over them.
+        if (!(ok = wait(&ctl->q_full, ic & 1u))) break;
+        const uint32_t qrow = smem_u32(smem + pf::kQ) + r * 128;
+        const int sw = r & 7;
+        float qv[64];
+        float qmax = 0.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t w0, w1, w2, w3;
+          ld_shared_v4(qrow + half * pf::kHalf + ((c ^ sw) << 4), w0, w1, w2, w3);
+          const uint32_t w[4] = {w0, w1, w2, w3};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            qv[8 * c + 2 * i] = __uint_as_float(w[i] << 16);
+            qv[8 * c + 2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+            qmax = fmax3(qmax, fabsf(qv[8 * c + 2 * i]), fabsf(qv[8 * c + 2 * i + 1]));
+          }
+        }
+        float rmax;
+        if (!(ok = exchange(qmax, false, &rmax))) break;
+        // 2^e with rmax 2^e in [128, 256); 1 for a row of zeros (or of non-finite values)
+        int e = 0;
+        if (rmax > 0.f && rmax <= 3.0e38f) e = 7 - (((__float_as_uint(rmax) >> 23) & 0xff) - 127);
+        e = max(-100, min(100, e));
+        const float sc = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+        sl_row = p.score_log2 * __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {  // 16-dim chunks 4 half + c of the three part rows
+          uint32_t hw[4], mw[4], lw[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint32_t hh = 0, mm = 0, ll = 0;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const float a0 = qv[16 * c + 4 * i + 2 * j] * sc;
+              const float a1 = qv[16 * c + 4 * i + 2 * j + 1] * sc;
+              const uint16_t h2 = f32x2_to_e4m3x2(a0, a1);
+              float h0, h1;
+              e4m3x2_to_f32x2(h2, h0, h1);
+              const float r0 = a0 - h0, r1 = a1 - h1;
+              const uint16_t m2 = f32x2_to_e4m3x2(r0, r1);
+              float m0, m1;
+              e4m3x2_to_f32x2(m2, m0, m1);
+              const uint16_t l2 = f32x2_to_e4m3x2(r0 - m0, r1 - m1);
+              hh |= static_cast<uint32_t>(h2) << (16 * j);
+              mm |= static_cast<uint32_t>(m2) << (16 * j);
+              ll |= static_cast<uint32_t>(l2) << (16 * j);
+            }
+            hw[i] = hh;
+            mw[i] = mm;
+            lw[i] = ll;
+          }
+          const uint32_t off = (((4 * half + c) ^ sw) << 4);
+          st_shared_v4(qrow + off, hw[0], hw[1], hw[2], hw[3]);
+          st_shared_v4(qrow + pf::kHalf + off, mw[0], mw[1], mw[2], mw[3]);
+          st_shared_v4(qrow + 2 * pf::kHalf + off, lw[0], lw[1], lw[2], lw[3]);
+        }
+        fence_proxy_async_smem();  // before the S MMAs read the parts
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->q_ready);
+      }
       // This thread's columns of S.  S of a slice is read into registers and the buffer
       // handed back (s_free) before the slice's P is worked out; a quarter with no row of the
       // run reads nothing and leaves its rows of P alone (their O rows are never read).
       const uint32_t s_cols = tl + pf::kSCol + hc;
-      bool ok = true;
-      for (int jj = 0; jj < I.nj; ++jj) {
+      for (int jj = 0; ok && jj < I.nj; ++jj) {
         const uint32_t g = tc + jj, b = g % pf::kPBufs;
         if (!(ok = wait(&ctl->s_full, g & 1u))) break;
         tc_fence_after();
@@ -533,7 +649,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))),
                             false, &mt)))
           break;
-        if (mt != -CUDART_INF_F) mt *= p.score_log2;
+        if (mt != -CUDART_INF_F) mt *= sl_row;
         bool rescale = false;
         float m_new = m_used;
         if (!seen) {
@@ -542,7 +658,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             m_new = mt;
             seen = true;
           }
-        } else if (mt > m_used + pf::kRescaleLog2) {
+        } else if (mt > m_used + (kFp8 ? pf::kRescaleLog2Fp8 : pf::kRescaleLog2)) {
           m_new = mt;
           rescale = true;
         }
@@ -560,10 +676,42 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         // The pairs of keys go through Blackwell's two-wide fp32 instructions (the scale-and-shift,
         // the row sums, the lo parts), each lane rounded as the scalar one would be.
         const uint32_t p_cols = tl + pf::kPCol + b * 128u + hc;
-        const f32x2 sl2 = f2_pack(p.score_log2, p.score_log2), mn2 = f2_pack(-m_new, -m_new);
+        // E4M3: P is made 2^8 times larger (kept under 448 by the rescale threshold), so that
+        // its small values stay clear of E4M3's subnormal floor; l carries the same factor.
+        constexpr float kPShift = kFp8 ? 8.f : 0.f;
+        const f32x2 sl2 = f2_pack(sl_row, sl_row),
+                    mn2 = f2_pack(kPShift - m_new, kPShift - m_new);
         f32x2 rsum[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) rsum[i] = f2_pack(0.f, 0.f);
+        if constexpr (kFp8) {
+          // hi = e4m3(p), lo = e4m3(p - hi): for the thread's 64 keys, 16 columns of hi (four
+          // keys a column) at 16 half, and of lo at 32 + 16 half
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int q4 = 0; q4 < 16; ++q4) {
+            uint32_t hh = 0, ll = 0;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const int k0 = 4 * q4 + 2 * j;
+              float a0, a1;
+              f2_unpack(f2_fma(f2_pack(x[k0], x[k0 + 1]), sl2, mn2), a0, a1);
+              const float p0 = fast_exp2(a0), p1 = fast_exp2(a1);
+              rsum[(2 * q4 + j) & 3] = f2_add(rsum[(2 * q4 + j) & 3], f2_pack(p0, p1));
+              const uint16_t h2 = f32x2_to_e4m3x2(p0, p1);
+              float h0, h1;
+              e4m3x2_to_f32x2(h2, h0, h1);
+              const uint16_t l2 = f32x2_to_e4m3x2(p0 - h0, p1 - h1);
+              hh |= static_cast<uint32_t>(h2) << (16 * j);
+              ll |= static_cast<uint32_t>(l2) << (16 * j);
+            }
+            hi[q4] = hh;
+            lo[q4] = ll;
+          }
+          const uint32_t pc = tl + pf::kPCol + b * 128u + 16 * half;
+          tmem_st16(pc, hi);
+          tmem_st16(pc + 32, lo);
+        } else {
 #pragma unroll
         for (int c = 0; c < kC / 32; ++c) {
           uint32_t hi[16], lo[16];
@@ -585,6 +733,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           const uint32_t pc = p_cols + (c >> 1) * 64 + (c & 1) * 16;
           tmem_st16(pc, hi);
           tmem_st16(pc + 32, lo);
+        }
         }
         float rs0, rs1, rs2, rs3, rs4, rs5, rs6, rs7;
         f2_unpack(rsum[0], rs0, rs1);
@@ -631,7 +780,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       const bool split = I.ns > 1;
       const uint32_t g_last = tc + I.nj - 1;
       const int sw = half ? warp - 4 : warp - 2;  // softmax warp index 0..7
-      uint8_t* stage = smem + pf::kStage + sw * (32 * kOC * 4);
+      uint8_t* stage = smem + kL.stage + sw * (32 * kOC * 4);
       const bool have =
           ok && live && wait(&ctl->o_done[g_last % pf::kPBufs], (g_last / pf::kPBufs) & 1u);
       // O may take the next item's P V once every softmax warp has read it.  A warp with no
@@ -653,12 +802,13 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           tmem_ld32(tl + pf::kOCol + oc + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&o[c * 32]));
         tmem_wait_ld();
         release_o();
-        const float inv = (row_ok && l > 0.f) ? 1.f / l : 0.f;
+        // E4M3: O and l both carry P's factor 2^8, and V its scale
+        const float inv = (row_ok && l > 0.f) ? (kFp8 ? p.v_out_scale : 1.f) / l : 0.f;
         const bool bf16 = p.out_bf16 && !split;   // partials are fp32
         if (split && half == 0 && row_ok)
           p.part_lse[(static_cast<int64_t>(I.t0 + tok) * p.num_q_heads + I.h * G + r % G) *
                          p.pmax + I.k] =
-              (seen && l > 0.f) ? m_used + __log2f(l) : -CUDART_INF_F;
+              (seen && l > 0.f) ? m_used + __log2f(l) - (kFp8 ? 8.f : 0.f) : -CUDART_INF_F;
         if (!bf16) {
           constexpr int CH = kOC / 4;   // 16-byte chunks of the thread's row part
 #pragma unroll
@@ -743,11 +893,12 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
 
 namespace {
 
-template <int D>
+template <int D, bool kFp8>
 cudaError_t launch_prefill_grid(const AttnArgs& a, const PrefillParams& p, const CUtensorMap& qmap,
                                 const CUtensorMap& kmap, const CUtensorMap& vmap) {
+  constexpr pf::Layout kL(kFp8);
   LaunchInfo li;
-  cudaError_t e = launch_info(prefill_kernel<D>, pf::kThreads, pf::kSmemBytes, &li);
+  cudaError_t e = launch_info(prefill_kernel<D, kFp8>, pf::kThreads, kL.smem, &li);
   if (e != cudaSuccess) return e;
   // at most one CTA per SM (shared memory); the plan decides how many of them work
   const int64_t upper =
@@ -756,8 +907,8 @@ cudaError_t launch_prefill_grid(const AttnArgs& a, const PrefillParams& p, const
        a.num_seqs);
   const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(upper, li.sms));
   if (a.pf_before && a.pf_after) cudaEventRecord(a.pf_before, a.stream);
-  e = launch_dependent(prefill_kernel<D>, dim3(static_cast<unsigned>(grid)), dim3(pf::kThreads),
-                       pf::kSmemBytes, a.stream, qmap, kmap, vmap, p);
+  e = launch_dependent(prefill_kernel<D, kFp8>, dim3(static_cast<unsigned>(grid)),
+                       dim3(pf::kThreads), kL.smem, a.stream, qmap, kmap, vmap, p);
   if (a.pf_before && a.pf_after) cudaEventRecord(a.pf_after, a.stream);
   return e;
 }
@@ -782,16 +933,21 @@ cudaError_t launch_prefill(const AttnArgs& a, const int32_t* item_start, const i
   p.group = a.num_q_heads / a.num_kv_heads;
   p.num_blocks = a.cache.num_blocks;
   p.out_bf16 = a.out_dtype == PA_BF16;
-  p.score_log2 = a.scale * 1.4426950408889634f;
+  const bool fp8 = a.cache.cache_dtype == PA_FP8_E4M3;
+  // E4M3 pools: K's scale folds into the scores, V's into the output
+  p.score_log2 = a.scale * 1.4426950408889634f * (fp8 ? a.cache.k_scale : 1.f);
+  p.v_out_scale = fp8 ? a.cache.v_scale : 1.f;
   p.wait_ns = a.wait_ns;
   p.skip_copy = a.skip_copy;
   p.span = a.span ? a.span + 2 : nullptr;
   p.part_lse = scratch.part_lse;
   p.part_o = scratch.part_o;
   p.pmax = scratch.pmax;
-  // head_dim 128: whole-tile 4-D copies; 64: the 2-D pool view, whose 16-row box is the tile
-  if (a.head_dim == 64) return launch_prefill_grid<64>(a, p, maps.q3, maps.k2, maps.v2);
-  return launch_prefill_grid<128>(a, p, maps.q3, maps.k4, maps.v4);
+  // bf16 head_dim 128: whole-tile 4-D copies; 64 and E4M3: the 2-D pool view, whose 16-row box
+  // is the tile
+  if (fp8) return launch_prefill_grid<128, true>(a, p, maps.q3, maps.k2, maps.v2);
+  if (a.head_dim == 64) return launch_prefill_grid<64, false>(a, p, maps.q3, maps.k2, maps.v2);
+  return launch_prefill_grid<128, false>(a, p, maps.q3, maps.k4, maps.v4);
 }
 
 }  // namespace pa

@@ -182,6 +182,19 @@ def test_prefill_chunks_head_dim_64(hq, hkv, out):
     _check_small(w, torch.bfloat16 if out == "bf16" else torch.float32)
 
 
+@pytest.mark.parametrize("hq,hkv,scale,out", [(32, 8, None, "f32"), (16, 16, None, "f32"),
+                                               (32, 4, 1.0, "f32"), (32, 8, None, "bf16")])
+def test_prefill_chunks_e4m3(hq, hkv, scale, out):
+    """E4M3 pools' chunks on the tensor-core tiles (f8f6f4 MMAs: q in three E4M3 parts with a
+    per-row scale, P in two parts scaled by 2^8, K and V as stored): chunks with and without a
+    cached prefix, a tile cut along the keys (7,000 keys), a five-token verify run and decodes
+    beside them; stale slots hold NaN patterns; scale 1 gives scores of sd ~11 nats."""
+    w = make_workload([700, 17, 7000, 300, 90, 3000], [200, 17, 200, 5, 1, 1], num_q_heads=hq,
+                      num_kv_heads=hkv, head_dim=128, cache_dtype="fp8_e4m3", seed=hq + hkv + 3,
+                      pool_fill="nan", scale=scale)
+    _check_small(w, torch.bfloat16 if out == "bf16" else torch.float32)
+
+
 def test_large_v_values_keep_their_precision():
     """V values far outside the N(0,1) range (+-65536, beyond what fp16 can hold, and 65280)
     in tensor-core tiles: P V stays exact (bf16 hi + lo parts of P against bf16 V), so the
