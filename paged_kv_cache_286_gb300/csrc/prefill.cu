@@ -8,15 +8,17 @@
 // Decoding": the draft tokens are checked in one pass); every run of more than 16 tokens or
 // more than 16 (token x head) rows comes here.
 //
-// Design (GB300 / sm_103a; bf16 K/V, head_dim 128):
+// Design (GB300 / sm_103a; written for bf16 K/V of head_dim 128, with instances for head_dim 64
+// and for E4M3 pools described at the end):
 //  * A tile is 128 rows, a row being (query token, q head of the GQA group), so the tile's
 //    queries share every K/V tile they read.  One work item is a tile over a range of 128-key
 //    slices: the tiles of very long runs are cut along the keys into several items
 //    (prefill_splits), each writing a normalised partial and its log-sum-exp into the
 //    workspace's split-KV arrays, which the merge kernel combines like the split-KV
 //    partitions.  Persistent CTAs (one per SM, as many as the plan gives this kernel) take
-//    items longest-first from an atomic counter; the V producer claims the CTA's next item while
-//    the current one runs.
+//    items from an atomic counter in the order the plan gives (runs by their longest item,
+//    longest first; within a run the last, longest tiles first); warp 0 claims the CTA's next
+//    item while the current one runs.
 //  * The pool is viewed by a 4-D tensor map as (64 columns, 8 rows, 2 column halves, 8-row
 //    groups), so that one TMA copy brings a whole 16 x 128 (block, kv head) tile: 8 copies per
 //    128 keys for K (lanes of warp 0, which also loads the q tile) and 8 for V (warp 6), into
@@ -58,6 +60,16 @@
 //    the plan gives this kernel end at once, and the split-KV kernel launches onto the rest.
 //  * Every wait is bounded; on expiry the CTA records PA_DEVERR_TIMEOUT, stops, lets the copies
 //    and MMAs it issued finish (bounded waits again) and frees its tensor memory.
+//  * head_dim 64: one 64-column q half, the (block, kv head) tiles of 2 KiB by one 2-D box of the
+//    pool (16 rows x 128 bytes) each, S from four MMAs, P V with N = 64 into 64 O columns.
+//  * E4M3 pools (head_dim 128): the MMAs are kind::f8f6f4, whose operands are both 8-bit, so
+//    K and V are read as stored (2 KiB tiles, one 2-D box each) while q and P are split into
+//    E4M3 parts.  The softmax warps turn the bf16 q tile into three parts (hi, mid, lo of q
+//    times a per-row power of two that puts the row's max in [128, 256)), whose three S MMAs
+//    per 32 dims accumulate into one S; P, made 2^8 times larger to keep small values clear of
+//    E4M3's subnormal floor, is written as hi and lo parts, and the lazy rescale threshold is
+//    2^0.5 so that it stays under 448.  k_scale and the row's q scale go into the scores,
+//    v_scale into the output.
 #include <math_constants.h>
 
 #include <algorithm>
