@@ -161,12 +161,23 @@ WsLayout workspace_layout(int32_t S, int32_t T, int32_t Hq, int32_t Hkv, int32_t
   const int64_t tpt = std::max(1, kRowsPerTile / std::max(1, G));
   const int64_t qtiles = (std::max<int64_t>(1, std::min(max_q, kDecodeMaxQuery)) + tpt - 1) / tpt;
   const int64_t maxblk = (std::max(1, max_ctx) + kBlockSize - 1) / kBlockSize;
-  // Largest partition that still yields enough work items to fill the GPU; a partition never
-  // has fewer than 8 blocks (2 per warp).
+  // Largest partition of 32 or fewer blocks that still yields enough work items to fill the
+  // GPU; a partition never has fewer than 8 blocks (2 per warp).
   int32_t pblk = 8;
   for (int32_t cand : {32, 16}) {
     const int64_t items = int64_t(S) * Hkv * qtiles * ((maxblk + cand - 1) / cand);
     if (items >= 1200) {
+      pblk = cand;
+      break;
+    }
+  }
+  // Long contexts take longer partitions, up to 128 blocks (the split-KV kernel's 4 warps
+  // hold one table entry per lane), while the longest sequence still has 8 of them and about
+  // 1,000 items remain: 16 x 32K tokens go from 32 to 128 blocks, with a quarter of the
+  // partials to write and merge.
+  for (int32_t cand : {128, 64}) {
+    const int64_t items = int64_t(S) * Hkv * qtiles * ((maxblk + cand - 1) / cand);
+    if (cand > pblk && cand <= maxblk / 8 && items >= 1000) {
       pblk = cand;
       break;
     }

@@ -1105,6 +1105,8 @@ cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const PoolMa
                                         a.max_query_len);
   p.heads_per_item = hpi;
   p.pblk = (fp8_cache && ws.pblk <= 32) ? ws.pblk * 2 : ws.pblk;
+  // a warp holds the table entries of its blocks of a partition one per lane
+  if (p.pblk > kDecodeWarps * 32) return cudaErrorInvalidValue;
   p.pmax = ws.pmax;
   const bool prefill = use_prefill && prefill_path_enabled(a.cache, a.num_q_heads,
                                                           a.num_kv_heads);
