@@ -285,22 +285,28 @@ class DeviceWorkload:
 
     def has_prefill(self) -> bool:
         """Whether the step launches the tensor-core prefill-tile kernel: query runs of more than
-        16 tokens or of more than 16 (token x head) rows, over a bf16 pool with head_dim 128
-        and a group that divides 128."""
+        16 tokens or of more than 16 (token x head) rows, over a bf16 pool with head_dim 128 or
+        64 or an E4M3 pool with head_dim 128, and a group that divides 128."""
         w = self.w
         g = w.num_q_heads // w.num_kv_heads
-        return ((w.max_query_len > 16 or w.max_query_len * g > 16) and w.cache_dtype == "bf16"
-                and w.head_dim == 128 and 128 % g == 0)
+        built = ((w.cache_dtype == "bf16" and w.head_dim in (64, 128))
+                 or (w.cache_dtype == "fp8_e4m3" and w.head_dim == 128))
+        return ((w.max_query_len > 16 or w.max_query_len * g > 16) and built
+                and g <= 8 and 128 % g == 0)
 
     def launches_per_step(self) -> int:
         """Our kernels one step launches: the append, the plan, the split-KV attention, the LSE
         merge when the workspace carries split partials, and the tensor-core prefill kernel
-        when the step holds chunks of more than 16 queries over a bf16 pool with head_dim 128."""
+        when the step holds chunks it serves (has_prefill)."""
         w = self.w
         size = self.pa.attention_workspace_size(w.num_seqs, w.num_tokens, w.num_q_heads,
                                                 w.num_kv_heads, w.head_dim, w.max_context_len,
                                                 w.max_query_len)
-        no_partials = 256 + 2 * (((4 * (w.num_seqs + 1) + 255) // 256) * 256)
+
+        def up(x):
+            return (x + 255) // 256 * 256
+        # the header and the four per-sequence arrays: more means split partials
+        no_partials = 256 + 3 * up(4 * (w.num_seqs + 1)) + up(4 * max(w.num_seqs, 1))
         return 3 + (1 if size > no_partials else 0) + (1 if self.has_prefill() else 0)
 
 

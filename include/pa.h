@@ -147,11 +147,11 @@ size_t pa_attention_workspace_size(int32_t num_seqs, int32_t num_q_tokens, int32
  * log2(e)-prescaled logits.
  * Kernels: every kernel of the call runs on `stream`, each launched early (programmatic
  * dependent launch) and waiting for what it reads: a plan, then, with a bf16 pool of head_dim
- * 128 or 64 and query runs of more than 16 tokens or more than 16 (token x q head) rows, the
- * tensor-core prefill tiles on the part of the SMs the plan gives them, the split-KV kernel on
- * the rest, and the merge of split sequences.  Work enqueued on `stream` after the call sees
- * all of it complete.  The call records no event and creates no stream, so it can be captured
- * into a CUDA graph like any kernel launch. */
+ * 128 or 64 or an E4M3 pool of head_dim 128 and query runs of more than 16 tokens or more than
+ * 16 (token x q head) rows, the tensor-core prefill tiles on the part of the SMs the plan gives
+ * them, the split-KV kernel on the rest, and the merge of split sequences.
+ * Work enqueued on `stream` after the call sees all of it complete.  The call records no event
+ * and creates no stream, so it can be captured into a CUDA graph like any kernel launch. */
 pa_status pa_attention(const void* q, int32_t num_q_tokens, const void* k_cache,
                        const void* v_cache, const pa_cache_desc* cache,
                        const int32_t* block_tables, int32_t max_blocks_per_seq,
@@ -179,8 +179,9 @@ pa_status pa_attention(const void* q, int32_t num_q_tokens, const void* k_cache,
  *                 `stream`, this call's PA_DEVERR_* bits (0 for a step with nothing to do).  It
  *                 is written only when the call returns PA_OK; a call rejected on the host
  *                 changes neither *error_word nor the scratch array.
- * The first call on a device looks up the scratch array's device address (once per device, with
- * that device current); make that first call before any stream capture.  Every call shares the
+ * Each call looks up the scratch array's device address in the current context
+ * (cudaGetSymbolAddress); the first lookup in a context may load the library's device code, so
+ * make the first call before any stream capture.  Every call shares the
  * one array and overwrites it, starting from a cleared header: calls whose GPU work overlaps
  * (other streams, other threads) race on it and must be serialised by the caller. */
 pa_status pa_attention_noalloc(const void* q, int32_t num_q_tokens, const void* k_cache,

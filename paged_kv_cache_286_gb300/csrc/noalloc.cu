@@ -11,10 +11,9 @@
 // This entry point keeps that scratch in one file-scope device array of
 // PA_NOALLOC_SCRATCH_BYTES bytes, which every GPU that loads the library holds until the process
 // exits.  Host code must not use the array's name as a device address (on the host it is only a
-// stand-in symbol); the device address is fetched once per device with cudaGetSymbolAddress,
-// with that device current, on the first call made on the device.
+// stand-in symbol); the device address is fetched with cudaGetSymbolAddress on every call, in
+// the context current at the call.
 #include <cstdio>
-#include <mutex>
 
 #include "pa_common.cuh"
 #include "pa_internal.h"
@@ -23,24 +22,13 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mutex;
-void* g_noalloc_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device (set up once per device).
+// Device address of the scratch array in the current context.  It is looked up on every call
+// rather than kept: after cudaDeviceReset the next context places the array anew.
 cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* ptr = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (!g_noalloc_ptr[dev]) {
-    void* ptr = nullptr;
-    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    g_noalloc_ptr[dev] = ptr;
-  }
-  *out = g_noalloc_ptr[dev];
+  *out = ptr;
   return cudaSuccess;
 }
 

@@ -57,7 +57,7 @@ constexpr float kLazyRescaleLog2 = 8.f;  // softmax base moves only past 2^8 gro
 // span many 128-key slices would make one item set the kernel's critical path (the 512-token
 // chunk after a 2,048-token prefix: about 20 slices per tile), so every tile of such a run is
 // cut along the keys into ns items of about equal length, each writing a normalised partial
-// and its log-sum-exp; the last of them to finish merges.  A run splits when even its first
+// and its log-sum-exp, which the merge kernel combines.  A run splits when even its first
 // tile spans at least kSplitSlices slices per split, into at most kMaxSplits items, and only
 // when the workspace holds that many partials per row (pmax).
 constexpr int kSplitSlices = 24;
