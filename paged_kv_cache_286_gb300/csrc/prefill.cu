@@ -22,30 +22,32 @@
 //  * The pool is viewed by a 4-D tensor map as (64 columns, 8 rows, 2 column halves, 8-row
 //    groups), so that one TMA copy brings a whole 16 x 128 (block, kv head) tile: 8 copies per
 //    128 keys for K (lanes of warp 0, which also loads the q tile) and 8 for V (warp 6), into
-//    three-stage rings.  One SM's TMA unit is limited by the number of copies rather than their
+//    two-stage rings.  One SM's TMA unit is limited by the number of copies rather than their
 //    bytes, so whole-tile copies halve the copy time of a slice.  In shared memory a block's
 //    tile is [2 row groups][2 halves][8 rows][128 bytes] with the 128-byte swizzle, i.e. 8-key
 //    groups 2 KiB apart and the column halves 1 KiB apart, which the MMA descriptors express
 //    as strides.
-//  * tcgen05.mma, each issued from one thread: warp 1 S = Q K^T into a TMEM buffer (128 x 128
-//    fp32), warp 7 O += P V into another, with P read from TMEM and V from shared memory
+//  * tcgen05.mma, each issued from one thread: warp 1 S = Q K^T into one of two TMEM buffers
+//    (128 x 128 fp32), warp 7 O += P V, with P read from TMEM and V from shared memory
 //    (MN-major).  With one issuing thread for both, every wait of that thread sat between
-//    two groups of MMAs while the tensor pipe ran dry; with two, each waits on its own.  The softmax threads write P as bf16 hi and lo parts (keys 0-63: hi in
-//    columns 0-31, lo in 32-63; keys 64-127 likewise in 64-127; P V is exact to ~2^-16 like
-//    the decode path) into one of two P buffers.  They read each S into registers and hand
-//    the buffer back at once, so S of slice j+1 is computed while the softmax works on slice
-//    j, and the softmax never waits for the P V of the slice before to free a buffer.  TMEM:
-//    S 128 columns, P 2 x 128, O 128.
-//  * Softmax, two threads per row (TMEM lane), one for keys (and O columns) 0-63 in warps 2-5
-//    and one for 64-127 in warps 8-11: each reads its half row of S from TMEM once, masks keys
-//    beyond the row's position, keeps the running max in the log2 domain (set by the first
-//    slice that shows the row a key) and rescales O in TMEM only when the max grows by more
-//    than 2^8 (the final division uses the same max, so the result is exact), and finally
-//    divides O by the row sum.  The two threads of a row agree on its max, and at the end add
-//    their sums, through a shared-memory slot and an mbarrier of the pair.  A warp can only
-//    reach the lane quarter of its own SM sub-partition; the per-slice work of a row is
-//    bound by instruction latency rather than issue, and the second warp on each
-//    sub-partition hides it (whole rows on one warp each took a quarter longer per slice).
+//    two groups of MMAs while the tensor pipe ran dry; with two, each waits on its own.  The
+//    softmax threads write P over the S they have read, as bf16 hi and lo parts (keys 0-63: hi
+//    in columns 0-31, lo in 32-63; keys 64-127 likewise in 64-127; P V is exact to ~2^-16 like
+//    the decode path), so S of slice j+1 is computed into the other buffer while the softmax
+//    works on slice j.  TMEM: S / P 2 x 128 columns, and two O accumulators of 128: keys 0-63
+//    of every slice add into one, keys 64-127 into the other.
+//  * Softmax, two threads per row (TMEM lane), one for keys 0-63 in warps 2-5 and one for
+//    64-127 in warps 8-11, each an online softmax of its own: it reads its half row of S from
+//    TMEM once, masks keys beyond the row's position, keeps its running max in the log2 domain
+//    (set by the first slice that shows it a key) and rescales its O accumulator in TMEM only
+//    when that max grows by more than 2^8 (the final division uses the same max, so the
+//    result is exact).  The two threads of a row meet only at the end of the item, through a
+//    shared-memory slot and an mbarrier of the pair: the larger max, the factor of each
+//    accumulator, the row sum; then each thread divides its output columns of the two scaled
+//    accumulators by the sum.  A warp can only reach the lane quarter of its own SM
+//    sub-partition; the per-slice work of a row is bound by instruction latency rather than
+//    issue, and the second warp on each sub-partition hides it (whole rows on one warp each
+//    took a quarter longer per slice).
 //  * V rows past the last valid key (stale slots, possibly NaN) are zeroed in shared memory
 //    before P V reads them (by the P V issuer's warp); K there only feeds masked scores.
 //  * The epilogue stages each warp's rows in a region of its own (swizzled) and writes whole
@@ -85,7 +87,7 @@ namespace pf {
 constexpr int kRows = 128;
 constexpr int kKeys = 128;
 constexpr int kStages = 2;   // K and V ring depth
-constexpr int kPBufs = 2;    // P buffers in TMEM, after the S buffer
+constexpr int kPBufs = 2;    // S / P buffers in TMEM (a slice's P is written over its S)
 constexpr int kHalf = 16384;  // one 64-column half of the q tile (bf16), or one E4M3 q part
 constexpr int kStageBytes = 65536;
 constexpr int kXBufs = 3;
@@ -116,8 +118,9 @@ constexpr int kThreads = 384;
 constexpr int kSoftmaxThreads = 256;
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSCol = 0, kPCol = 128, kOCol = kPCol + kPBufs * 128;
-static_assert(kOCol + 128 == kTmemCols, "TMEM columns");
+// S / P buffer b at columns 128 b; then one O accumulator for each half of the keys
+constexpr uint32_t kOCol = kPBufs * 128;
+static_assert(kOCol + 2 * 128 == kTmemCols, "TMEM columns");
 constexpr float kRescaleLog2 = 8.f;
 constexpr float kRescaleLog2Fp8 = 0.5f;  // E4M3 P (times 2^8) stays under 2^8.5 < 448
 }  // namespace pf
@@ -130,7 +133,7 @@ struct PfItem {
 
 struct PfCtl {
   uint64_t q_full, k_full[pf::kStages], k_empty[pf::kStages], v_full[pf::kStages],
-      v_empty[pf::kStages], s_full, s_free, p_full[pf::kPBufs], o_done[pf::kPBufs], drain[2],
+      v_empty[pf::kStages], s_full[pf::kPBufs], p_full[pf::kPBufs], o_done[pf::kPBufs], drain[2],
       q_empty, o_free, item_full[2], item_empty[2], q_ready;
   uint32_t tmem_base;
   int abort_flag;
@@ -238,12 +241,11 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       mbar_init(&ctl->v_full[i], 1);
       mbar_init(&ctl->v_empty[i], 1);
     }
-    // S of slice g+1 is issued only once the softmax has read S of slice g (s_free), and the
-    // softmax writes P of slice g+2 only once P V of slice g has run: one p_full / o_done per
-    // P buffer keeps every waiter within one phase of its barrier
-    mbar_init(&ctl->s_full, 1);
-    mbar_init(&ctl->s_free, pf::kSoftmaxThreads);
+    // S of slice g goes into buffer g % 2 once the P V of slice g - 2 has read the P there
+    // (o_done); the softmax writes the slice's P over its S (p_full).  One s_full / p_full /
+    // o_done per buffer keeps every waiter within one phase of its barrier.
     for (int i = 0; i < pf::kPBufs; ++i) {
+      mbar_init(&ctl->s_full[i], 1);
       mbar_init(&ctl->p_full[i], pf::kSoftmaxThreads);
       mbar_init(&ctl->o_done[i], 1);
     }
@@ -405,14 +407,16 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       if (!ok) break;
     } else if (warp == 1) {
       // ------------------------------------------------------------- S issuer -----------
-      // S of slice jj into the S buffer once the softmax has read S of jj - 1 out of it.
+      // S of slice g into buffer g % 2 once the P V of slice g - 2 has read its P there.
       const uint32_t id_s = kFp8 ? idesc_e4m3_f32(128, 128, false) : idesc_bf16_f32(128, 128, false);
       const uint32_t q_addr = smem_u32(smem + pf::kQ);
       // E4M3 pools: the softmax warps turn the bf16 q tile into three E4M3 parts first
       bool ok = wait(kFp8 ? &ctl->q_ready : &ctl->q_full, ic & 1u);
       for (int jj = 0; ok && jj < I.nj; ++jj) {
-        const uint32_t g = tc + jj, st = g % pf::kStages;
-        if (g > 0 && !(ok = wait(&ctl->s_free, (g - 1) & 1u))) break;
+        const uint32_t g = tc + jj, st = g % pf::kStages, b = g % pf::kPBufs;
+        if (g >= pf::kPBufs &&
+            !(ok = wait(&ctl->o_done[b], ((g - pf::kPBufs) / pf::kPBufs) & 1u)))
+          break;
         if (!(ok = wait(&ctl->k_full[st], (g / pf::kStages) & 1u))) break;
         tc_fence_after();
         if (lane == 0) {
@@ -424,7 +428,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             for (int ks = 0; ks < 4; ++ks)
 #pragma unroll
               for (int part = 0; part < 3; ++part)
-                tc_mma_f8(tmem + pf::kSCol,
+                tc_mma_f8(tmem + b * 128u,
                           smem_desc_sw128(q_addr + part * pf::kHalf + ks * 32, 16, 1024),
                           smem_desc_sw128(k_addr + ks * 32, 16, 1024), id_s, ks > 0 || part > 0);
           } else {
@@ -434,11 +438,11 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             // groups 2 KiB apart), or one half (64: 8-key groups 1 KiB apart)
             const uint32_t qa = q_addr + (ks >> 2) * pf::kHalf + (ks & 3) * 32;
             const uint32_t kb = k_addr + (ks >> 2) * 1024 + (ks & 3) * 32;
-            tc_mma_bf16(tmem + pf::kSCol, smem_desc_sw128(qa, 16, 1024),
+            tc_mma_bf16(tmem + b * 128u, smem_desc_sw128(qa, 16, 1024),
                         smem_desc_sw128(kb, 16, D == 128 ? 2048 : 1024), id_s, ks > 0);
           }
           }
-          tc_commit(&ctl->s_full);
+          tc_commit(&ctl->s_full[b]);
           tc_commit(&ctl->k_empty[st]);
         }
         __syncwarp();
@@ -483,20 +487,23 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           // P of keys 16 ks .. 16 ks + 15: the hi parts of keys 0-63 in columns 0-31 of the
           // buffer and their lo parts in 32-63; keys 64-127 the same in columns 64-127.  V of
           // those keys: block ks of the stage, MN-major (head_dim 128: the column halves 1 KiB
-          // apart, 8-key groups 2 KiB apart; 64: one half, 8-key groups 1 KiB apart).
-          auto p_col = [&](int ks) {
-            return tmem + pf::kPCol + b * 128u + (ks >> 2) * 64u + (ks & 3) * 8u;
-          };
+          // apart, 8-key groups 2 KiB apart; 64: one half, 8-key groups 1 KiB apart).  Keys
+          // 0-63 go into one O accumulator and keys 64-127 into the other: the two halves of a
+          // row keep their own running max.
+          auto p_col = [&](int ks) { return tmem + b * 128u + (ks >> 2) * 64u + (ks & 3) * 8u; };
+          auto o_acc = [&](int h) { return tmem + pf::kOCol + h * 128u; };
           if constexpr (kFp8) {
             // P as E4M3 hi and lo parts, 4 keys a column: keys 32 ks .. 32 ks + 31 in columns
-            // 8 ks .. 8 ks + 7 (hi) and 32 + 8 ks .. (lo); V of those keys: blocks 2 ks and
-            // 2 ks + 1 of the stage, MN-major rows of 128 bytes (8-key groups 1 KiB apart)
-            const uint32_t pb = tmem + pf::kPCol + b * 128u;
+            // 64 (ks / 2) + 8 (ks % 2) .. + 7 (hi) and 16 further (lo), inside the columns of
+            // their half's S; V of those keys: blocks 2 ks and 2 ks + 1 of the stage, MN-major
+            // rows of 128 bytes (8-key groups 1 KiB apart)
+            const uint32_t pb = tmem + b * 128u;
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
               const uint64_t vd = smem_desc_sw128(v_addr + ks * 2 * kBlk, 1024, 1024);
-              tc_mma_f8_ts(tmem + pf::kOCol, pb + ks * 8, vd, id_pv, jj > 0 || ks > 0);
-              tc_mma_f8_ts(tmem + pf::kOCol, pb + 32 + ks * 8, vd, id_pv, true);
+              const uint32_t pc = pb + (ks >> 1) * 64u + (ks & 1) * 8u;
+              tc_mma_f8_ts(o_acc(ks >> 1), pc, vd, id_pv, jj > 0 || (ks & 1) > 0);
+              tc_mma_f8_ts(o_acc(ks >> 1), pc + 16u, vd, id_pv, true);
             }
           } else {
           auto v_desc = [&](int ks) {
@@ -504,10 +511,10 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           };
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            tc_mma_bf16_ts(tmem + pf::kOCol, p_col(ks), v_desc(ks), id_pv, jj > 0 || ks > 0);
+            tc_mma_bf16_ts(o_acc(ks >> 2), p_col(ks), v_desc(ks), id_pv, jj > 0 || (ks & 3) > 0);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            tc_mma_bf16_ts(tmem + pf::kOCol, p_col(ks) + 32u, v_desc(ks), id_pv, true);
+            tc_mma_bf16_ts(o_acc(ks >> 2), p_col(ks) + 32u, v_desc(ks), id_pv, true);
           }
           tc_commit(&ctl->o_done[b]);
           tc_commit(&ctl->v_empty[st]);
@@ -621,23 +628,22 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->q_ready);
       }
-      // This thread's columns of S.  S of a slice is read into registers and the buffer
-      // handed back (s_free) before the slice's P is worked out; a quarter with no row of the
-      // run reads nothing and leaves its rows of P alone (their O rows are never read).
-      const uint32_t s_cols = tl + pf::kSCol + hc;
+      // The two halves of a row (keys 0-63 and 64-127 of every slice) run their own online
+      // softmax, each with its own running max, row sum and O accumulator, and meet only at the
+      // end of the item.  This thread's columns of S are read into registers and its P is
+      // written over them; a quarter with no row of the run reads nothing and leaves its rows
+      // of P alone (their O rows are never read).
       for (int jj = 0; ok && jj < I.nj; ++jj) {
         const uint32_t g = tc + jj, b = g % pf::kPBufs;
-        if (!(ok = wait(&ctl->s_full, g & 1u))) break;
+        if (!(ok = wait(&ctl->s_full[b], (g / pf::kPBufs) & 1u))) break;
         tc_fence_after();
         if (!live) {
-          mbar_arrive(&ctl->s_free);
           mbar_arrive(&ctl->p_full[b]);
           continue;
         }
+        const uint32_t s_cols = tl + b * 128u + hc;
         uint32_t sv[kC];
         tmem_ld_row<kC>(s_cols, sv);
-        tc_fence_before();
-        mbar_arrive(&ctl->s_free);
         // keys 0..kmax of this thread's columns are visible
         const int kmax = row_ok ? row_pos - (I.j0 + jj) * pf::kKeys - half * 64 : -1;
         // raw scores, masked keys -inf; the row max is taken on them (the scale is positive)
@@ -656,11 +662,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         }
 #pragma unroll
         for (int i = 0; i < kC; i += 2) mx[(i >> 1) & 7] = fmax3(mx[(i >> 1) & 7], x[i], x[i + 1]);
-        float mt;
-        if (!(ok = exchange(fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))),
-                            false, &mt)))
-          break;
+        float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         if (mt != -CUDART_INF_F) mt *= sl_row;
         bool rescale = false;
         float m_new = m_used;
@@ -675,19 +678,13 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           rescale = true;
         }
         const float alpha = rescale ? fast_exp2(m_used - m_new) : 1.f;
-        // The P buffer is free once the P V of two slices back has run (long since, as a
-        // rule: it was handed over a slice ago).
-        if (g >= pf::kPBufs &&
-            !(ok = wait(&ctl->o_done[b], ((g - pf::kPBufs) / pf::kPBufs) & 1u)))
-          break;
-        tc_fence_after();
-        // probabilities 2^(s * scale * log2 e - m); for every 64 keys, bf16 hi parts into their
-        // columns 0..31 and lo parts into 32..63.  The split is by truncation, on the integer
+        // probabilities 2^(s * scale * log2 e - m); for the thread's 64 keys, bf16 hi parts
+        // into its columns 0..31 and lo parts into 32..63.  The split is by truncation, on the integer
         // pipes: hi keeps the upper 16 bits of p, lo = p - hi exactly in fp32, and lo is
         // truncated in turn, so hi + lo = p within 2^-14 relative.
         // The pairs of keys go through Blackwell's two-wide fp32 instructions (the scale-and-shift,
         // the row sums, the lo parts), each lane rounded as the scalar one would be.
-        const uint32_t p_cols = tl + pf::kPCol + b * 128u + hc;
+        const uint32_t p_cols = s_cols;
         // E4M3: P is made 2^8 times larger (kept under 448 by the rescale threshold), so that
         // its small values stay clear of E4M3's subnormal floor; l carries the same factor.
         constexpr float kPShift = kFp8 ? 8.f : 0.f;
@@ -698,7 +695,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         for (int i = 0; i < 4; ++i) rsum[i] = f2_pack(0.f, 0.f);
         if constexpr (kFp8) {
           // hi = e4m3(p), lo = e4m3(p - hi): for the thread's 64 keys, 16 columns of hi (four
-          // keys a column) at 16 half, and of lo at 32 + 16 half
+          // keys a column) at its columns 0..15, and of lo at 16..31
           uint32_t hi[16], lo[16];
 #pragma unroll
           for (int q4 = 0; q4 < 16; ++q4) {
@@ -720,9 +717,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             hi[q4] = hh;
             lo[q4] = ll;
           }
-          const uint32_t pc = tl + pf::kPCol + b * 128u + 16 * half;
-          tmem_st16(pc, hi);
-          tmem_st16(pc + 32, lo);
+          tmem_st16(p_cols, hi);
+          tmem_st16(p_cols + 16, lo);
         } else {
 #pragma unroll
         for (int c = 0; c < kC / 32; ++c) {
@@ -755,36 +751,51 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         const float rs = ((rs0 + rs1) + (rs2 + rs3)) + ((rs4 + rs5) + (rs6 + rs7));
         l = l * alpha + rs;
         if (__any_sync(0xffffffffu, rescale)) {
-          // O may be rescaled only once the previous P V has landed in it (a rescale needs a
-          // visible key in an earlier slice of the item, so jj > 0)
+          // this half's O accumulator (all D columns) moves to the new base once the previous
+          // P V has landed in it (a rescale needs a visible key in an earlier slice of the
+          // item, so jj > 0)
           if (!(ok = wait(&ctl->o_done[(g - 1) % pf::kPBufs], ((g - 1) / pf::kPBufs) & 1u)))
             break;
           tc_fence_after();
-          uint32_t o[kOC];
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tl + pf::kOCol + half * 128u + c * 32, o);
+            tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < kOC / 32; ++c)
-            tmem_ld32(tl + pf::kOCol + oc + c * 32,
-                      *reinterpret_cast<uint32_t(*)[32]>(&o[c * 32]));
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < kOC; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-#pragma unroll
-          for (int c = 0; c < kOC / 32; ++c)
-            tmem_st32(tl + pf::kOCol + oc + c * 32,
-                      *reinterpret_cast<uint32_t(*)[32]>(&o[c * 32]));
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tl + pf::kOCol + half * 128u + c * 32, o);
+          }
         }
         tmem_wait_st();
         m_used = m_new;
         tc_fence_before();
         mbar_arrive(&ctl->p_full[b]);
       }
-      // Epilogue: the thread's columns of O divided by the row sum (of both halves), to the
-      // output, or (a split tile) to the item's partial with its log-sum-exp in the log2
-      // domain, which the merge kernel combines after the split-KV kernel.
+      // Epilogue: the two halves of the row meet.  The row's base is the larger of theirs,
+      // f_a and f_b scale the two O accumulators (and row sums) to it; the thread's columns of
+      // O_a f_a + O_b f_b divided by the row sum go to the output, or (a split tile) to the
+      // item's partial with its log-sum-exp in the log2 domain, which the merge kernel
+      // combines after the split-KV kernel.  One of the two factors is 1 (the half with the
+      // larger base), so a thread needs the other's only when its own is 1: the max of the
+      // factors below 1 (-1 standing for 1) gives it.  Both threads of a row get the same
+      // factors and sum (a sum of two values does not depend on their order).
+      float f_a = 0.f, f_b = 0.f;
       if (ok && live) {
-        float lt;
-        ok = exchange(l, true, &lt);
+        const float m_h = seen ? m_used : -CUDART_INF_F;
+        float m_row = -CUDART_INF_F, f_lt1 = -1.f, lt = 0.f;
+        ok = exchange(m_h, false, &m_row);
+        const float f = m_h == m_row               ? 1.f
+                        : (m_h == -CUDART_INF_F) ? 0.f
+                                                 : fast_exp2(m_h - m_row);
+        if (ok) ok = exchange(f < 1.f ? f : -1.f, false, &f_lt1);
+        const float f_other = (f < 1.f || f_lt1 < 0.f) ? 1.f : f_lt1;
+        f_a = half == 0 ? f : f_other;
+        f_b = half == 0 ? f_other : f;
+        if (ok) ok = exchange(l * f, true, &lt);
         l = lt;
+        m_used = m_row;
+        seen = m_row != -CUDART_INF_F;
       }
       // Each warp stages its 32 rows in the (now idle) K stages, swizzled by row so that
       // neither the row-wise writes nor the chunk-wise reads conflict on banks, and then
@@ -813,6 +824,18 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         for (int c = 0; c < kOC / 32; ++c)
           tmem_ld32(tl + pf::kOCol + oc + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&o[c * 32]));
         tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < kOC; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f_a);
+#pragma unroll
+        for (int c = 0; c < kOC / 32; ++c) {
+          uint32_t ob[32];
+          tmem_ld32(tl + pf::kOCol + 128u + oc + c * 32, ob);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            o[c * 32 + i] = __float_as_uint(
+                fmaf(__uint_as_float(ob[i]), f_b, __uint_as_float(o[c * 32 + i])));
+        }
         release_o();
         // E4M3: O and l both carry P's factor 2^8, and V its scale
         const float inv = (row_ok && l > 0.f) ? (kFp8 ? p.v_out_scale : 1.f) / l : 0.f;
