@@ -224,7 +224,28 @@ __global__ void __launch_bounds__(1024) plan_kernel(const DecodeParams p) {
   // so that the CTAs taking items from the counter end close together.  A bitonic sort in
   // shared memory, padded to a power of two with entries that sort last.
   const int R = carry_s[3];
-  if (R > 1 && R <= kSortMax) {
+  if (R > 1 && R <= 256) {
+    // few runs: each thread counts the runs that go before its own (larger key, or the same
+    // key and a lower sequence: a strict order), one barrier instead of the sort's stages
+    int key = 0, val = 0, cnt = 0, rank = 0;
+    if (tid < R) {
+      key = sort_key[tid];
+      val = sort_val[tid];
+      cnt = sort_cnt[tid];
+      for (int j = 0; j < R; ++j) {
+        const int kj = sort_key[j];
+        rank += kj > key || (kj == key && sort_val[j] < val);
+      }
+    }
+    __syncthreads();
+    if (tid < R) {
+      sort_key[rank] = key;
+      sort_val[rank] = val;
+      sort_cnt[rank] = cnt;
+    }
+    __syncthreads();
+    for (int i = tid; i < R; i += 1024) p.pf_order[i] = sort_val[i];
+  } else if (R > 1 && R <= kSortMax) {
     int n2 = 2;
     while (n2 < R) n2 <<= 1;
     for (int i = R + tid; i < n2; i += 1024) {
