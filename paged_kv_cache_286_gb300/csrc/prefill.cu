@@ -48,8 +48,10 @@
 //    sub-partition; the per-slice work of a row is bound by instruction latency rather than
 //    issue, and the second warp on each sub-partition hides it (whole rows on one warp each
 //    took a quarter longer per slice).
-//  * V rows past the last valid key (stale slots, possibly NaN) are zeroed in shared memory
-//    before P V reads them (by the P V issuer's warp); K there only feeds masked scores.
+//  * Pool slots past the sequence's end (stale, possibly NaN) in its last loaded block are
+//    zeroed in shared memory before P V reads them (by the P V issuer's warp); blocks past the
+//    tile's last position are not loaded, and their rows keep older, finite V data (the ring
+//    starts zeroed) under P = 0.  K there only feeds masked scores.
 //  * The epilogue stages each warp's rows in a region of its own (swizzled) and writes whole
 //    rows per instruction, instead of one scattered 16-byte piece per row and instruction.
 //  * Items follow one another without a block-wide barrier: warp 0 claims the next item while
@@ -137,7 +139,7 @@ struct PfCtl {
       q_empty, o_free, item_full[2], item_empty[2], q_ready;
   uint32_t tmem_base;
   int abort_flag;
-  int v_zero_from[pf::kStages];
+  int v_zero_from[pf::kStages], v_zero_to[pf::kStages];
   uint32_t v_bad[pf::kStages];
   PfItem item[2];  // by the parity of the item count: warp 0 fills one while the other is read
 };
@@ -275,6 +277,10 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
   }
   int* xslot = reinterpret_cast<int*>(smem + kL.xslot);  // [kXBufs][kRows]
   for (int i = tid; i < pf::kXBufs * pf::kRows; i += pf::kThreads) xslot[i] = INT_MIN;
+  // the V ring starts zeroed: rows of blocks a slice does not load are then always finite
+  for (int i = tid; i < pf::kStages * kL.stage_stride / 16; i += pf::kThreads)
+    reinterpret_cast<uint4*>(smem + kL.v)[i] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
   if (warp == 1) tmem_alloc(&ctl->tmem_base, pf::kTmemCols);
   tc_fence_before();
   __syncthreads();
@@ -384,6 +390,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             // rows the P V issuer clears: keys past the last valid one, and bad blocks
             const int valid_end = min(I.L, I.nblk_tile * kBlockSize) - j * pf::kKeys;
             ctl->v_zero_from[st] = max(0, min(pf::kKeys, valid_end));
+            ctl->v_zero_to[st] =
+                max(0, min(pf::kKeys, I.nblk_tile * kBlockSize - j * pf::kKeys));
             ctl->v_bad[st] = badm;
             if (bytes) mbar_arrive_expect_tx(&ctl->v_full[st], bytes);
             else mbar_arrive(&ctl->v_full[st]);
@@ -465,18 +473,27 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         const uint32_t g = tc + jj, st = g % pf::kStages, b = g % pf::kPBufs;
         if (!wait(&ctl->v_full[st], (g / pf::kStages) & 1u)) break;
         uint8_t* vt = smem + kL.v + st * kL.stage_stride;
-        const int zf = ctl->v_zero_from[st];
+        const int zf = ctl->v_zero_from[st], zt = ctl->v_zero_to[st];
         const uint32_t badm = ctl->v_bad[st];
-        if (zf < pf::kKeys || badm) {
-          // clear the 128-byte rows (every column half) of keys that hold no valid value;
-          // key kk of the slice: block kk / 16, row group (kk / 8) % 2, row kk % 8
+        if (zf < zt || badm) {
+          // clear the 128-byte rows (every column half) of keys that hold no valid value: the
+          // pool slots past the sequence's end in its last loaded block, and the blocks with
+          // a bad id.  (Blocks past the tile's last position are not loaded; their rows keep
+          // older V data, finite since the ring starts zeroed and every stale slot that lands
+          // is cleared here, and P is 0 there.)  Key kk of the slice: block kk / 16, row group
+          // (kk / 8) % 2, row kk % 8.
           constexpr int kHalves = kBlk / 2048;  // 128-byte column halves of a key's row
-          for (int e = lane; e < pf::kKeys * kHalves * 8; e += 32) {
-            const int key = e / (kHalves * 8), half = (e >> 3) % kHalves, c16 = e & 7;
-            if (key >= zf || ((badm >> (key >> 4)) & 1u))
-              *reinterpret_cast<uint4*>(vt + (key >> 3) * (kHalves * 1024) + half * 1024 +
-                                        (key & 7) * 128 + c16 * 16) = make_uint4(0u, 0u, 0u, 0u);
-          }
+          auto clear_key = [&](int key, int e) {
+            const int half = (e >> 3) % kHalves, c16 = e & 7;
+            *reinterpret_cast<uint4*>(vt + (key >> 3) * (kHalves * 1024) + half * 1024 +
+                                      (key & 7) * 128 + c16 * 16) = make_uint4(0u, 0u, 0u, 0u);
+          };
+          for (int e = lane; e < (zt - zf) * kHalves * 8; e += 32) clear_key(zf + e / (kHalves * 8), e);
+          if (badm)
+            for (int e = lane; e < pf::kKeys * kHalves * 8; e += 32) {
+              const int key = e / (kHalves * 8);
+              if ((badm >> (key >> 4)) & 1u) clear_key(key, e);
+            }
           fence_proxy_async_smem();
           __syncwarp();
         }
