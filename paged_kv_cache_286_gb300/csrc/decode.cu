@@ -901,8 +901,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, (kFp8 && HPI > 1) ? 3 : 1)
 }
 
 // Eight loads of kPer consecutive floats each, issued back to back in one asm block (so that
-// they are in flight together whatever the register allocator prefers); the merge issues two
-// such blocks before it uses any of the sixteen results.
+// they are in flight together whatever the register allocator prefers) before the merge uses
+// any of the results.
 template <int kPer>
 __device__ __forceinline__ void load_batch8(const float* const (&src)[8], float (&v)[8][kPer]);
 
@@ -957,7 +957,7 @@ __device__ __forceinline__ void merge_row(const DecodeParams& p, int64_t rid, in
 #pragma unroll
   for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   constexpr int kPer = D / 32;  // columns per lane
-  constexpr int kBatch = 16;    // partitions whose loads are in flight together
+  constexpr int kBatch = 8;     // partitions whose loads are in flight together
   float acc[kPer];
 #pragma unroll
   for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
@@ -975,12 +975,11 @@ __device__ __forceinline__ void merge_row(const DecodeParams& p, int64_t rid, in
       float v[kBatch][kPer];
       // past the last partition a load repeats it (a written, finite partial) under a zero
       // weight, so the batch's loads are unconditional and go out back to back
-      const float* src[2][8];
+      const float* src[8];
 #pragma unroll
       for (int u = 0; u < kBatch; ++u)
-        src[u >> 3][u & 7] = po + static_cast<int64_t>(base + min(j0 + u, cnt - 1)) * D;
-      load_batch8<kPer>(src[0], *reinterpret_cast<float(*)[8][kPer]>(&v[0][0]));
-      load_batch8<kPer>(src[1], *reinterpret_cast<float(*)[8][kPer]>(&v[8][0]));
+        src[u] = po + static_cast<int64_t>(base + min(j0 + u, cnt - 1)) * D;
+      load_batch8<kPer>(src, v);
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
         const float wj = __shfl_sync(0xffffffffu, w, j0 + u);  // 0 past nparts
@@ -1006,9 +1005,9 @@ __device__ __forceinline__ void merge_row(const DecodeParams& p, int64_t rid, in
 // plan lists those rows (merge_start), and a grid of at most one resident wave strides over
 // them.
 template <int D>
-// (At least 2 CTAs per SM, i.e. up to 128 registers a thread: room for the sixteen loads in
-// flight, which a full-occupancy register budget of 32 would serialise.)
-__global__ void __launch_bounds__(256, 2) merge_kernel(const DecodeParams p) {
+// (At least 4 CTAs per SM, i.e. up to 64 registers a thread: room for the eight loads in flight
+// of a row, with twice the rows in flight of two CTAs per SM and sixteen loads.)
+__global__ void __launch_bounds__(256, 4) merge_kernel(const DecodeParams p) {
   grid_dependency_wait();  // the attention kernel's partials (and the plan) are complete
   const int lane = threadIdx.x & 31;
   const int total = p.merge_start[p.num_seqs];
