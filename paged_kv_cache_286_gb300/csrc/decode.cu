@@ -412,10 +412,11 @@ struct ItemInfo {
   int s, h, qt, part, t0, n, L, nparts, blk_begin, blk_end, pos_base, rows, valid, idx;
 };
 
-// The E4M3 two-head instance is held to 3 CTAs per SM (at most 170 registers a thread): it is
-// latency-bound, and its 2-stage rings leave room in shared memory for the third CTA.
+// Instances with 2-stage rings are held to 3 CTAs per SM (at most 170 registers a thread): the
+// kernel is latency-bound per SM, and the third CTA's warps, which the smaller rings leave room
+// for in shared memory, keep more blocks in flight.
 template <int D, bool kFp8, int NST, int RT, int HPI>
-__global__ void __launch_bounds__(kDecodeWarps * 32, (kFp8 && HPI > 1) ? 3 : 1)
+__global__ void __launch_bounds__(kDecodeWarps * 32, NST == 2 ? 3 : 1)
     decode_kernel(const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
   // RT row tiles of 8 rows: rows quad and quad + 8 of the m16 MMA (RT = 2 uses both halves).
@@ -1177,7 +1178,7 @@ cudaError_t launch_attention(const AttnArgs& a, const WsLayout& ws, const PoolMa
             : run_decode<128, true, 4, 1>(a, ws, p, kmap, vmap, before, after);
   else if (a.head_dim == 128)  // whole-tile 4-D copies
     e = rt2 ? run_decode<128, false, 3, 2>(a, ws, p, maps.k4, maps.v4, before, after)
-            : run_decode<128, false, 3, 1>(a, ws, p, maps.k4, maps.v4, before, after);
+            : run_decode<128, false, 2, 1>(a, ws, p, maps.k4, maps.v4, before, after);
   else
     e = rt2 ? run_decode<64, false, 4, 2>(a, ws, p, kmap, vmap, before, after)
             : run_decode<64, false, 4, 1>(a, ws, p, kmap, vmap, before, after);
