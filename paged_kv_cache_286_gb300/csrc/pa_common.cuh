@@ -28,8 +28,8 @@ struct WsHeader {
 // one 128-key slice of a 128-row prefill tile and the fixed time of one item (its first copies
 // and MMAs, and its output); the HBM bytes per microsecond one SM's split-KV CTAs stream; and
 // the chip's HBM bytes per microsecond.
-constexpr float kTileSliceUs = 1.4f;
-constexpr float kTileItemUs = 4.5f;
+constexpr float kTileSliceUs = 1.34f;
+constexpr float kTileItemUs = 3.5f;
 constexpr float kDecodeSmBytesPerUs = 7.5e4f;
 constexpr float kHbmBytesPerUs = 6.7e6f;
 
