@@ -27,27 +27,25 @@
 //    tile is [2 row groups][2 halves][8 rows][128 bytes] with the 128-byte swizzle, i.e. 8-key
 //    groups 2 KiB apart and the column halves 1 KiB apart, which the MMA descriptors express
 //    as strides.
-//  * tcgen05.mma, each issued from one thread: warp 1 S = Q K^T into one of two TMEM buffers
+//  * tcgen05.mma, each issued from one thread: warp 1 S = Q K^T into one of three TMEM buffers
 //    (128 x 128 fp32), warp 7 O += P V, with P read from TMEM and V from shared memory
 //    (MN-major).  With one issuing thread for both, every wait of that thread sat between
 //    two groups of MMAs while the tensor pipe ran dry; with two, each waits on its own.  The
 //    softmax threads write P over the S they have read, as bf16 hi and lo parts (keys 0-63: hi
 //    in columns 0-31, lo in 32-63; keys 64-127 likewise in 64-127; P V is exact to ~2^-16 like
-//    the decode path), so S of slice j+1 is computed into the other buffer while the softmax
-//    works on slice j.  TMEM: S / P 2 x 128 columns, and two O accumulators of 128: keys 0-63
-//    of every slice add into one, keys 64-127 into the other.
-//  * Softmax, two threads per row (TMEM lane), one for keys 0-63 in warps 2-5 and one for
-//    64-127 in warps 8-11, each an online softmax of its own: it reads its half row of S from
-//    TMEM once, masks keys beyond the row's position, keeps its running max in the log2 domain
-//    (set by the first slice that shows it a key) and rescales its O accumulator in TMEM only
-//    when that max grows by more than 2^8 (the final division uses the same max, so the
-//    result is exact).  The two threads of a row meet only at the end of the item, through a
-//    shared-memory slot and an mbarrier of the pair: the larger max, the factor of each
-//    accumulator, the row sum; then each thread divides its output columns of the two scaled
-//    accumulators by the sum.  A warp can only reach the lane quarter of its own SM
-//    sub-partition; the per-slice work of a row is bound by instruction latency rather than
-//    issue, and the second warp on each sub-partition hides it (whole rows on one warp each
-//    took a quarter longer per slice).
+//    the decode path), and S of slice j+3 goes into a buffer once the P V of slice j has read
+//    it, so the S MMAs run up to three slices ahead of the softmax.  TMEM: S / P 3 x 128
+//    columns, O 128.
+//  * Softmax, two threads per row (TMEM lane), one for keys (and O columns) 0-63 in warps 2-5
+//    and one for 64-127 in warps 8-11: each reads its half row of S from TMEM once, masks keys
+//    beyond the row's position, keeps the running max in the log2 domain (set by the first
+//    slice that shows the row a key) and rescales O in TMEM only when the max grows by more
+//    than 2^8 (the final division uses the same max, so the result is exact), and finally
+//    divides O by the row sum.  The two threads of a row agree on its max, and at the end add
+//    their sums, through a shared-memory slot and an mbarrier of the pair.  A warp can only
+//    reach the lane quarter of its own SM sub-partition; the per-slice work of a row is
+//    bound by instruction latency rather than issue, and the second warp on each
+//    sub-partition hides it (whole rows on one warp each took a quarter longer per slice).
 //  * Pool slots past the sequence's end (stale, possibly NaN) in its last loaded block are
 //    zeroed in shared memory before P V reads them (by the P V issuer's warp); blocks past the
 //    tile's last position are not loaded, and their rows keep older, finite V data (the ring
@@ -89,7 +87,7 @@ namespace pf {
 constexpr int kRows = 128;
 constexpr int kKeys = 128;
 constexpr int kStages = 2;   // K and V ring depth
-constexpr int kPBufs = 2;    // S / P buffers in TMEM (a slice's P is written over its S)
+constexpr int kPBufs = 3;    // S / P buffers in TMEM (a slice's P is written over its S)
 constexpr int kHalf = 16384;  // one 64-column half of the q tile (bf16), or one E4M3 q part
 constexpr int kStageBytes = 65536;
 constexpr int kXBufs = 3;
@@ -120,9 +118,9 @@ constexpr int kThreads = 384;
 constexpr int kSoftmaxThreads = 256;
 
 constexpr uint32_t kTmemCols = 512;
-// S / P buffer b at columns 128 b; then one O accumulator for each half of the keys
+// S / P buffer b at columns 128 b; then the O accumulator
 constexpr uint32_t kOCol = kPBufs * 128;
-static_assert(kOCol + 2 * 128 == kTmemCols, "TMEM columns");
+static_assert(kOCol + 128 == kTmemCols, "TMEM columns");
 constexpr float kRescaleLog2 = 8.f;
 constexpr float kRescaleLog2Fp8 = 0.5f;  // E4M3 P (times 2^8) stays under 2^8.5 < 448
 }  // namespace pf
@@ -243,7 +241,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       mbar_init(&ctl->v_full[i], 1);
       mbar_init(&ctl->v_empty[i], 1);
     }
-    // S of slice g goes into buffer g % 2 once the P V of slice g - 2 has read the P there
+    // S of slice g goes into buffer g % 3 once the P V of slice g - 3 has read the P there
     // (o_done); the softmax writes the slice's P over its S (p_full).  One s_full / p_full /
     // o_done per buffer keeps every waiter within one phase of its barrier.
     for (int i = 0; i < pf::kPBufs; ++i) {
@@ -415,7 +413,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       if (!ok) break;
     } else if (warp == 1) {
       // ------------------------------------------------------------- S issuer -----------
-      // S of slice g into buffer g % 2 once the P V of slice g - 2 has read its P there.
+      // S of slice g into buffer g % 3 once the P V of slice g - 3 has read its P there.
       const uint32_t id_s = kFp8 ? idesc_e4m3_f32(128, 128, false) : idesc_bf16_f32(128, 128, false);
       const uint32_t q_addr = smem_u32(smem + pf::kQ);
       // E4M3 pools: the softmax warps turn the bf16 q tile into three E4M3 parts first
@@ -504,11 +502,9 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           // P of keys 16 ks .. 16 ks + 15: the hi parts of keys 0-63 in columns 0-31 of the
           // buffer and their lo parts in 32-63; keys 64-127 the same in columns 64-127.  V of
           // those keys: block ks of the stage, MN-major (head_dim 128: the column halves 1 KiB
-          // apart, 8-key groups 2 KiB apart; 64: one half, 8-key groups 1 KiB apart).  Keys
-          // 0-63 go into one O accumulator and keys 64-127 into the other: the two halves of a
-          // row keep their own running max.
+          // apart, 8-key groups 2 KiB apart; 64: one half, 8-key groups 1 KiB apart).
           auto p_col = [&](int ks) { return tmem + b * 128u + (ks >> 2) * 64u + (ks & 3) * 8u; };
-          auto o_acc = [&](int h) { return tmem + pf::kOCol + h * 128u; };
+          const uint32_t o_acc = tmem + pf::kOCol;
           if constexpr (kFp8) {
             // P as E4M3 hi and lo parts, 4 keys a column: keys 32 ks .. 32 ks + 31 in columns
             // 64 (ks / 2) + 8 (ks % 2) .. + 7 (hi) and 16 further (lo), inside the columns of
@@ -519,8 +515,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             for (int ks = 0; ks < 4; ++ks) {
               const uint64_t vd = smem_desc_sw128(v_addr + ks * 2 * kBlk, 1024, 1024);
               const uint32_t pc = pb + (ks >> 1) * 64u + (ks & 1) * 8u;
-              tc_mma_f8_ts(o_acc(ks >> 1), pc, vd, id_pv, jj > 0 || (ks & 1) > 0);
-              tc_mma_f8_ts(o_acc(ks >> 1), pc + 16u, vd, id_pv, true);
+              tc_mma_f8_ts(o_acc, pc, vd, id_pv, jj > 0 || ks > 0);
+              tc_mma_f8_ts(o_acc, pc + 16u, vd, id_pv, true);
             }
           } else {
           auto v_desc = [&](int ks) {
@@ -528,10 +524,10 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           };
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            tc_mma_bf16_ts(o_acc(ks >> 2), p_col(ks), v_desc(ks), id_pv, jj > 0 || (ks & 3) > 0);
+            tc_mma_bf16_ts(o_acc, p_col(ks), v_desc(ks), id_pv, jj > 0 || ks > 0);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            tc_mma_bf16_ts(o_acc(ks >> 2), p_col(ks) + 32u, v_desc(ks), id_pv, true);
+            tc_mma_bf16_ts(o_acc, p_col(ks) + 32u, v_desc(ks), id_pv, true);
           }
           tc_commit(&ctl->o_done[b]);
           tc_commit(&ctl->v_empty[st]);
@@ -645,11 +641,9 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->q_ready);
       }
-      // The two halves of a row (keys 0-63 and 64-127 of every slice) run their own online
-      // softmax, each with its own running max, row sum and O accumulator, and meet only at the
-      // end of the item.  This thread's columns of S are read into registers and its P is
-      // written over them; a quarter with no row of the run reads nothing and leaves its rows
-      // of P alone (their O rows are never read).
+      // This thread's columns of S are read into registers and its P is written over them; a
+      // quarter with no row of the run reads nothing and leaves its rows of P alone (their O
+      // rows are never read).
       for (int jj = 0; ok && jj < I.nj; ++jj) {
         const uint32_t g = tc + jj, b = g % pf::kPBufs;
         if (!(ok = wait(&ctl->s_full[b], (g / pf::kPBufs) & 1u))) break;
@@ -679,8 +673,11 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         }
 #pragma unroll
         for (int i = 0; i < kC; i += 2) mx[(i >> 1) & 7] = fmax3(mx[(i >> 1) & 7], x[i], x[i + 1]);
-        float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        float mt;
+        if (!(ok = exchange(fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))),
+                            false, &mt)))
+          break;
         if (mt != -CUDART_INF_F) mt *= sl_row;
         bool rescale = false;
         float m_new = m_used;
@@ -768,51 +765,36 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         const float rs = ((rs0 + rs1) + (rs2 + rs3)) + ((rs4 + rs5) + (rs6 + rs7));
         l = l * alpha + rs;
         if (__any_sync(0xffffffffu, rescale)) {
-          // this half's O accumulator (all D columns) moves to the new base once the previous
-          // P V has landed in it (a rescale needs a visible key in an earlier slice of the
-          // item, so jj > 0)
+          // this thread's columns of O move to the new base once the previous P V has landed
+          // in it (a rescale needs a visible key in an earlier slice of the item, so jj > 0)
           if (!(ok = wait(&ctl->o_done[(g - 1) % pf::kPBufs], ((g - 1) / pf::kPBufs) & 1u)))
             break;
           tc_fence_after();
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tl + pf::kOCol + half * 128u + c * 32, o);
-            tmem_wait_ld();
+          uint32_t o[kOC];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tl + pf::kOCol + half * 128u + c * 32, o);
-          }
+          for (int c = 0; c < kOC / 32; ++c)
+            tmem_ld32(tl + pf::kOCol + oc + c * 32,
+                      *reinterpret_cast<uint32_t(*)[32]>(&o[c * 32]));
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < kOC; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+#pragma unroll
+          for (int c = 0; c < kOC / 32; ++c)
+            tmem_st32(tl + pf::kOCol + oc + c * 32,
+                      *reinterpret_cast<uint32_t(*)[32]>(&o[c * 32]));
         }
         tmem_wait_st();
         m_used = m_new;
         tc_fence_before();
         mbar_arrive(&ctl->p_full[b]);
       }
-      // Epilogue: the two halves of the row meet.  The row's base is the larger of theirs,
-      // f_a and f_b scale the two O accumulators (and row sums) to it; the thread's columns of
-      // O_a f_a + O_b f_b divided by the row sum go to the output, or (a split tile) to the
-      // item's partial with its log-sum-exp in the log2 domain, which the merge kernel
-      // combines after the split-KV kernel.  One of the two factors is 1 (the half with the
-      // larger base), so a thread needs the other's only when its own is 1: the max of the
-      // factors below 1 (-1 standing for 1) gives it.  Both threads of a row get the same
-      // factors and sum (a sum of two values does not depend on their order).
-      float f_a = 0.f, f_b = 0.f;
+      // Epilogue: the thread's columns of O divided by the row sum (of both halves), to the
+      // output, or (a split tile) to the item's partial with its log-sum-exp in the log2
+      // domain, which the merge kernel combines after the split-KV kernel.
       if (ok && live) {
-        const float m_h = seen ? m_used : -CUDART_INF_F;
-        float m_row = -CUDART_INF_F, f_lt1 = -1.f, lt = 0.f;
-        ok = exchange(m_h, false, &m_row);
-        const float f = m_h == m_row               ? 1.f
-                        : (m_h == -CUDART_INF_F) ? 0.f
-                                                 : fast_exp2(m_h - m_row);
-        if (ok) ok = exchange(f < 1.f ? f : -1.f, false, &f_lt1);
-        const float f_other = (f < 1.f || f_lt1 < 0.f) ? 1.f : f_lt1;
-        f_a = half == 0 ? f : f_other;
-        f_b = half == 0 ? f_other : f;
-        if (ok) ok = exchange(l * f, true, &lt);
+        float lt;
+        ok = exchange(l, true, &lt);
         l = lt;
-        m_used = m_row;
-        seen = m_row != -CUDART_INF_F;
       }
       // Each warp stages its 32 rows in the (now idle) K stages, swizzled by row so that
       // neither the row-wise writes nor the chunk-wise reads conflict on banks, and then
@@ -841,18 +823,6 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         for (int c = 0; c < kOC / 32; ++c)
           tmem_ld32(tl + pf::kOCol + oc + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&o[c * 32]));
         tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < kOC; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f_a);
-#pragma unroll
-        for (int c = 0; c < kOC / 32; ++c) {
-          uint32_t ob[32];
-          tmem_ld32(tl + pf::kOCol + 128u + oc + c * 32, ob);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            o[c * 32 + i] = __float_as_uint(
-                fmaf(__uint_as_float(ob[i]), f_b, __uint_as_float(o[c * 32 + i])));
-        }
         release_o();
         // E4M3: O and l both carry P's factor 2^8, and V its scale
         const float inv = (row_ok && l > 0.f) ? (kFp8 ? p.v_out_scale : 1.f) / l : 0.f;
