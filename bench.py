@@ -473,8 +473,16 @@ def run_reference(args):
     budget = 150.0 / max(1, args.steps + args.warmup)   # whole run within a few minutes
     run = OracleRunner(args.config, cores)
     try:
-        dt1 = run.pool.apply(_shard_run, ((args.config, 0, 1),))[0]
-        k = max(1, int(0.8 * budget / max(dt1, 1e-3)))
+        # one sequence per process with every process busy (the per-sequence time under
+        # contention, after a first pass that builds the shards), then as many sequences per
+        # process as fit the step's budget, and no more than twice the workload's sequences
+        # over all processes (a larger sample only repeats its sequences and multiplies the
+        # memory every process builds)
+        from synthetic.workloads import config_lengths
+        S = len(config_lengths(args.config)[0])
+        run.step(1)
+        dt1 = run.step(1)[0]
+        k = max(1, min(max(1, 2 * S // cores), int(0.8 * budget / max(dt1, 1e-3))))
         times, nbytes, toks = [], 0, 0
         for i in range(args.warmup + args.steps):
             wall, nb, tk = run.step(k)
