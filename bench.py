@@ -464,6 +464,14 @@ def cpu_baseline(config_id: int, seconds: float):
             "sample_1core": f"{k} sequences in one process, {dt1:.1f} s"}
 
 
+def reference_sample_size(num_seqs: int, cores: int, budget_s: float, seq_s: float) -> int:
+    """Sequences per process for one reference-arm step: as many as fit 0.8 of the step's
+    budget at the contended per-sequence time, and no more than twice the workload's sequences
+    over all processes (a larger sample only repeats its sequences and multiplies the memory
+    every process builds); at least one."""
+    return max(1, min(max(1, 2 * num_seqs // max(1, cores)), int(0.8 * budget_s / max(seq_s, 1e-3))))
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -482,7 +490,7 @@ def run_reference(args):
         S = len(config_lengths(args.config)[0])
         run.step(1)
         dt1 = run.step(1)[0]
-        k = max(1, min(max(1, 2 * S // cores), int(0.8 * budget / max(dt1, 1e-3))))
+        k = reference_sample_size(S, cores, budget, dt1)
         times, nbytes, toks = [], 0, 0
         for i in range(args.warmup + args.steps):
             wall, nb, tk = run.step(k)

@@ -56,3 +56,15 @@ def test_attended_pairs_and_prefill_flops_by_brute_force():
     assert tiled == [1, 2, 3]
     # QK^T and PV: 2 x 2 flops per (query, key) pair, head dim and q head
     assert bench.prefill_flops(w) == 4 * d * hq * sum(pairs[s] for s in tiled)
+
+
+def test_reference_arm_sample_is_bounded():
+    # as many sequences per process as fit 0.8 of the step's budget at the contended time ...
+    assert bench.reference_sample_size(num_seqs=64, cores=16, budget_s=6.0, seq_s=0.7) == 6
+    # ... but never more than twice the workload's sequences over all processes, however fast
+    # one sequence is (an uncapped sample only repeats sequences and grows every process)
+    assert bench.reference_sample_size(num_seqs=64, cores=16, budget_s=50.0, seq_s=0.01) == 8
+    assert bench.reference_sample_size(num_seqs=64, cores=8, budget_s=50.0, seq_s=0.01) == 16
+    # and always at least one
+    assert bench.reference_sample_size(num_seqs=4, cores=16, budget_s=0.1, seq_s=5.0) == 1
+    assert bench.reference_sample_size(num_seqs=64, cores=16, budget_s=1.0, seq_s=0.0) == 8
